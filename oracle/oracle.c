@@ -1,0 +1,280 @@
+/*
+ * oracle.c -- plain, slow, single-threaded CPU oracle for the fp32/int32 axis
+ * reductions (full-vector sum/max/min, per-row sum/max/min with accum, dense
+ * and ragged rows, and TCOLPROD column products).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path (the CUDA library and
+ * its Python binding) includes, links or calls this file.  Only the test
+ * suite, the smoke check and the benchmark's CPU-baseline leg may load it.  It
+ * shares no header, helper, table or constant with the CUDA sources.
+ *
+ * Every function below is the plain definition of its result, written out in
+ * index order with no blocking, no reordering and no parallelism:
+ *   - sums accumulate in double (and also report sum |x| for tolerances);
+ *   - max / min compare the fp32 values directly (exact in any order);
+ *   - fp32 column products accumulate in double and round to fp32 once;
+ *   - int32 column products multiply in uint32, i.e. wrap modulo 2^32.
+ *
+ * Sources (cited by page title and section):
+ *   [TVM]  Apache TVM docs, "reduction -> sm100_packed": sections "Algorithm"
+ *          (sum of a 1-D float32 vector; max / min), "How inputs change the
+ *          algorithm" (accum folds the old dst value into the first
+ *          accumulator slot), "Demonstration program" (B == sum(A)).
+ *   [PTO]  pto-isa docs, "TCOLPROD": "Math Interpretation"
+ *          (dst[0,j] = prod_{i<R} src[i,j]) and "Constraints" (returns early
+ *          when R == 0 or C == 0).
+ *
+ * Readings where the pages are silent (each one is also listed in the design doc):
+ *   - An empty dense input has no max / min: status -1 (error).  An empty
+ *     ragged row folds nothing, so its max is -inf and its min +inf (with
+ *     accum the old dst value survives); an empty sum is 0.
+ *   - The early return of TCOLPROD leaves dst untouched (no identity written).
+ *
+ * Parity status: every function here is pinned by the CPU tests (page-given
+ * 32-element check, closed forms, exact-arithmetic brute force, invariants).
+ *
+ * Return value of every function: 0 on success, -1 on invalid arguments.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#define ORC_OK 0
+#define ORC_EINVAL (-1)
+
+/* ---------------------------------------------------------------- full --- */
+
+/* [TVM] "Algorithm", sum: the scalar sum of a 1-D float32 vector.
+ * *sum = sum_i x[i] and *abs_sum = sum_i |x[i]|, both in double. */
+int orc_full_sum(const float *x, int64_t n, double *sum, double *abs_sum)
+{
+    if (n < 0 || (n > 0 && !x) || !sum || !abs_sum)
+        return ORC_EINVAL;
+    double s = 0.0, a = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        s += (double)x[i];
+        a += fabs((double)x[i]);
+    }
+    *sum = s;
+    *abs_sum = a;
+    return ORC_OK;
+}
+
+/* [TVM] "Algorithm", max / min: the largest (smallest) element, in fp32.
+ * An empty vector has no extreme: -1. */
+int orc_full_max(const float *x, int64_t n, float *out)
+{
+    if (n <= 0 || !x || !out)
+        return ORC_EINVAL;
+    float m = x[0];
+    for (int64_t i = 1; i < n; ++i)
+        if (x[i] > m)
+            m = x[i];
+    *out = m;
+    return ORC_OK;
+}
+
+int orc_full_min(const float *x, int64_t n, float *out)
+{
+    if (n <= 0 || !x || !out)
+        return ORC_EINVAL;
+    float m = x[0];
+    for (int64_t i = 1; i < n; ++i)
+        if (x[i] < m)
+            m = x[i];
+    *out = m;
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------ row core --- */
+
+/* Sum of seg[0..len), started from `init` (accum: the old dst value goes into
+ * the first accumulator slot, [TVM] "How inputs change the algorithm"). */
+static double seg_sum(const float *seg, int64_t len, double init, double *abs_out,
+                      double abs_init)
+{
+    double s = init, a = abs_init;
+    for (int64_t i = 0; i < len; ++i) {
+        s += (double)seg[i];
+        a += fabs((double)seg[i]);
+    }
+    *abs_out = a;
+    return s;
+}
+
+static float seg_max(const float *seg, int64_t len, float init)
+{
+    float m = init;
+    for (int64_t i = 0; i < len; ++i)
+        if (seg[i] > m)
+            m = seg[i];
+    return m;
+}
+
+static float seg_min(const float *seg, int64_t len, float init)
+{
+    float m = init;
+    for (int64_t i = 0; i < len; ++i)
+        if (seg[i] < m)
+            m = seg[i];
+    return m;
+}
+
+/* ---------------------------------------------------------- dense rows --- */
+
+/* Row r is x[r*len .. r*len+len) (row-major, leading dimension len).
+ * out[r] = (accum ? dst_old[r] : 0) + sum of row r, in double;
+ * abs_out[r] = (accum ? |dst_old[r]| : 0) + sum of |row r|. */
+int orc_rows_sum(const float *x, int64_t rows, int64_t len, int accum,
+                 const float *dst_old, double *out, double *abs_out)
+{
+    if (rows < 0 || len < 0 || (rows > 0 && (!out || !abs_out)) ||
+        (rows > 0 && len > 0 && !x) || (accum && rows > 0 && !dst_old))
+        return ORC_EINVAL;
+    for (int64_t r = 0; r < rows; ++r) {
+        double init = accum ? (double)dst_old[r] : 0.0;
+        double ainit = accum ? fabs((double)dst_old[r]) : 0.0;
+        out[r] = seg_sum(x + r * len, len, init, &abs_out[r], ainit);
+    }
+    return ORC_OK;
+}
+
+/* out[r] = max over row r (folded with dst_old[r] when accum).  A dense row
+ * of length 0 has no max: -1. */
+int orc_rows_max(const float *x, int64_t rows, int64_t len, int accum,
+                 const float *dst_old, float *out)
+{
+    if (rows < 0 || len < 0 || (rows > 0 && (!out || !x)) ||
+        (accum && rows > 0 && !dst_old) || (rows > 0 && len == 0))
+        return ORC_EINVAL;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *seg = x + r * len;
+        float m = seg_max(seg + 1, len - 1, seg[0]);
+        if (accum && dst_old[r] > m)
+            m = dst_old[r];
+        out[r] = m;
+    }
+    return ORC_OK;
+}
+
+int orc_rows_min(const float *x, int64_t rows, int64_t len, int accum,
+                 const float *dst_old, float *out)
+{
+    if (rows < 0 || len < 0 || (rows > 0 && (!out || !x)) ||
+        (accum && rows > 0 && !dst_old) || (rows > 0 && len == 0))
+        return ORC_EINVAL;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float *seg = x + r * len;
+        float m = seg_min(seg + 1, len - 1, seg[0]);
+        if (accum && dst_old[r] < m)
+            m = dst_old[r];
+        out[r] = m;
+    }
+    return ORC_OK;
+}
+
+/* --------------------------------------------------------- ragged rows --- */
+
+/* Row r is x[off[r] .. off[r+1]) with off[0] = 0, off non-decreasing and
+ * off[rows] the number of values.  Offsets that break this are rejected. */
+static int check_offsets(const int64_t *off, int64_t rows)
+{
+    if (off[0] != 0)
+        return ORC_EINVAL;
+    for (int64_t r = 0; r < rows; ++r)
+        if (off[r + 1] < off[r])
+            return ORC_EINVAL;
+    return ORC_OK;
+}
+
+int orc_ragged_sum(const float *x, const int64_t *off, int64_t rows, int accum,
+                   const float *dst_old, double *out, double *abs_out)
+{
+    if (rows < 0 || !off || (rows > 0 && (!out || !abs_out)) ||
+        (accum && rows > 0 && !dst_old))
+        return ORC_EINVAL;
+    if (check_offsets(off, rows) != ORC_OK || (off[rows] > 0 && !x))
+        return ORC_EINVAL;
+    for (int64_t r = 0; r < rows; ++r) {
+        double init = accum ? (double)dst_old[r] : 0.0;
+        double ainit = accum ? fabs((double)dst_old[r]) : 0.0;
+        out[r] = seg_sum(x + off[r], off[r + 1] - off[r], init, &abs_out[r], ainit);
+    }
+    return ORC_OK;
+}
+
+/* An empty ragged row folds nothing: -inf for max (the old dst value with
+ * accum). */
+int orc_ragged_max(const float *x, const int64_t *off, int64_t rows, int accum,
+                   const float *dst_old, float *out)
+{
+    if (rows < 0 || !off || (rows > 0 && !out) || (accum && rows > 0 && !dst_old))
+        return ORC_EINVAL;
+    if (check_offsets(off, rows) != ORC_OK || (off[rows] > 0 && !x))
+        return ORC_EINVAL;
+    for (int64_t r = 0; r < rows; ++r) {
+        float init = accum ? dst_old[r] : -INFINITY;
+        out[r] = seg_max(x + off[r], off[r + 1] - off[r], init);
+    }
+    return ORC_OK;
+}
+
+int orc_ragged_min(const float *x, const int64_t *off, int64_t rows, int accum,
+                   const float *dst_old, float *out)
+{
+    if (rows < 0 || !off || (rows > 0 && !out) || (accum && rows > 0 && !dst_old))
+        return ORC_EINVAL;
+    if (check_offsets(off, rows) != ORC_OK || (off[rows] > 0 && !x))
+        return ORC_EINVAL;
+    for (int64_t r = 0; r < rows; ++r) {
+        float init = accum ? dst_old[r] : INFINITY;
+        out[r] = seg_min(x + off[r], off[r + 1] - off[r], init);
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------- TCOLPROD --- */
+
+/* [PTO] "Math Interpretation": dst[0,j] = prod_{i=0}^{R-1} src[i,j] for
+ * 0 <= j < C, src row-major R x C.  The product of each column is taken in
+ * double, in row order, and written both as double (out_d, may be NULL) and
+ * rounded once to fp32 (out_f, may be NULL).  [PTO] "Constraints": R == 0 or
+ * C == 0 returns early and writes nothing. */
+int orc_colprod_f32(const float *x, int64_t R, int64_t C, float *out_f, double *out_d)
+{
+    if (R < 0 || C < 0)
+        return ORC_EINVAL;
+    if (R == 0 || C == 0)
+        return ORC_OK;
+    if (!x || (!out_f && !out_d))
+        return ORC_EINVAL;
+    for (int64_t j = 0; j < C; ++j) {
+        double p = 1.0;
+        for (int64_t i = 0; i < R; ++i)
+            p *= (double)x[i * C + j];
+        if (out_d)
+            out_d[j] = p;
+        if (out_f)
+            out_f[j] = (float)p;
+    }
+    return ORC_OK;
+}
+
+/* Same definition for int32: products wrap modulo 2^32 (done in uint32 so
+ * that overflow is defined), then reinterpret as int32. */
+int orc_colprod_i32(const int32_t *x, int64_t R, int64_t C, int32_t *out)
+{
+    if (R < 0 || C < 0)
+        return ORC_EINVAL;
+    if (R == 0 || C == 0)
+        return ORC_OK;
+    if (!x || !out)
+        return ORC_EINVAL;
+    for (int64_t j = 0; j < C; ++j) {
+        uint32_t p = 1u;
+        for (int64_t i = 0; i < R; ++i)
+            p *= (uint32_t)x[i * C + j];
+        out[j] = (int32_t)p;
+    }
+    return ORC_OK;
+}

@@ -1,0 +1,314 @@
+"""Pins of the CPU oracle to facts fixed outside the oracle itself.
+
+Each check uses one of: the worked check a page gives (32-element sum), a
+closed form, exact-arithmetic brute force on tiny inputs (``math.fsum``,
+``fractions.Fraction``, Python big integers), or an invariant of the
+definition.  They are chosen so that a dropped term, a wrong index or stride,
+a wrong sign, a transposed operand or a mishandled remainder in the oracle
+fails at least one of them.
+"""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from conftest import golden_lines
+
+
+def _grid_uniform(rng, n, lo=-1.0, hi=1.0):
+    """fp32 values on the 2**-23 grid in [lo, hi), none exactly zero.
+
+    Sums of up to 2**20 such values are exact in double, so the oracle's
+    double sum must equal math.fsum bit for bit.
+    """
+    k = rng.integers(int(lo * 2**23), int(hi * 2**23), size=n)
+    k[k == 0] = 1
+    return (k.astype(np.float64) * 2.0**-23).astype(np.float32)
+
+
+# ------------------------------------------------------------ page check
+
+def test_sum32_page_demo():
+    """Apache TVM docs, "reduction -> sm100_packed", "Demonstration program":
+    B == sum(A) for a 32-element float32 vector (values A[i] = i)."""
+    rows = dict((r[0], r[1:]) for r in golden_lines("sm100_packed_demo_sum32.txt"))
+    n = int(rows["n"][0])
+    a = np.array([float(v) for v in rows["A"]], np.float32)
+    assert a.size == n == 32
+    s, ab = oracle.full_sum(a)
+    assert s == float(rows["B"][0]) == 496.0
+    assert ab == 496.0
+
+
+# ------------------------------------------------------------ full sum
+
+@pytest.mark.parametrize("n", [1, 2, 7, 8, 9, 31, 32, 33, 1000, 4097, 1 << 20])
+def test_sum_arange_closed_form(n):
+    """sum_{i<n} i = n(n-1)/2, exact (all values and partial sums < 2**53)."""
+    a = np.arange(n, dtype=np.float32)
+    s, ab = oracle.full_sum(a)
+    assert s == n * (n - 1) // 2
+    assert ab == n * (n - 1) // 2
+
+
+def test_sum_negated_arange():
+    """Sign check: sum of -i is -n(n-1)/2 while sum |x| stays n(n-1)/2."""
+    a = -np.arange(100, dtype=np.float32)
+    s, ab = oracle.full_sum(a)
+    assert s == -4950.0 and ab == 4950.0
+
+
+def test_sum_bruteforce_fsum():
+    """Every length 0..64 (covers chunk-of-8 remainders 0..7) against fsum."""
+    rng = np.random.default_rng(11)
+    for n in range(0, 65):
+        for _ in range(3):
+            a = _grid_uniform(rng, n, -4.0, 4.0)
+            s, ab = oracle.full_sum(a)
+            assert s == math.fsum(float(v) for v in a)
+            assert ab == math.fsum(abs(float(v)) for v in a)
+
+
+def test_sum_empty_is_zero():
+    s, ab = oracle.full_sum(np.zeros(0, np.float32))
+    assert s == 0.0 and ab == 0.0
+
+
+def test_sum_accumulates_in_double():
+    """2**24 + 1 + 1 + ... is lost in an fp32 accumulator but not in double."""
+    a = np.ones(1001, np.float32)
+    a[0] = 2.0**24
+    s, _ = oracle.full_sum(a)
+    assert s == 2.0**24 + 1000
+
+
+# ------------------------------------------------------------ full max/min
+
+def test_max_min_position_sweep():
+    """The extreme is found at every index of every length 1..64."""
+    rng = np.random.default_rng(12)
+    for n in range(1, 65):
+        base = _grid_uniform(rng, n, -1.0, 1.0)
+        for p in range(n):
+            a = base.copy()
+            a[p] = 3.5
+            assert oracle.full_max(a) == np.float32(3.5)
+            a[p] = -3.5
+            assert oracle.full_min(a) == np.float32(-3.5)
+
+
+def test_max_min_bruteforce_and_duality():
+    rng = np.random.default_rng(13)
+    for n in (1, 5, 8, 13, 40, 257):
+        a = _grid_uniform(rng, n, -2.0, 2.0)
+        assert oracle.full_max(a) == max(a.tolist())
+        assert oracle.full_min(a) == min(a.tolist())
+        assert oracle.full_max(a) == -oracle.full_min(-a)
+
+
+def test_max_min_empty_rejected():
+    with pytest.raises(oracle.OracleError):
+        oracle.full_max(np.zeros(0, np.float32))
+    with pytest.raises(oracle.OracleError):
+        oracle.full_min(np.zeros(0, np.float32))
+
+
+# ------------------------------------------------------------ dense rows
+
+@pytest.mark.parametrize("rows,length", [(1, 1), (3, 7), (5, 8), (4, 9), (7, 31), (6, 40), (2, 100)])
+def test_rows_bruteforce(rows, length):
+    rng = np.random.default_rng(rows * 100 + length)
+    x = _grid_uniform(rng, rows * length, -4.0, 4.0).reshape(rows, length)
+    s, ab = oracle.rows("sum", x, rows, length)
+    mx = oracle.rows("max", x, rows, length)
+    mn = oracle.rows("min", x, rows, length)
+    for r in range(rows):
+        row = [float(v) for v in x[r]]
+        assert s[r] == math.fsum(row)
+        assert ab[r] == math.fsum(abs(v) for v in row)
+        assert mx[r] == max(row)
+        assert mn[r] == min(row)
+
+
+def test_rows_accum_closed_form():
+    """Rows of ones: sum with accum = dst_old + len (exact); the old value is
+    folded in once, not per element; max/min fold dst_old as one more value."""
+    rows, length = 6, 37
+    x = np.ones((rows, length), np.float32)
+    dst = np.array([-0.5, 0.25, 100.0, -100.0, 1.5, 0.75], np.float32)
+    s, ab = oracle.rows("sum", x, rows, length, accum=True, dst_old=dst)
+    assert (s == dst.astype(np.float64) + length).all()
+    assert (ab == np.abs(dst.astype(np.float64)) + length).all()
+    mx = oracle.rows("max", x, rows, length, accum=True, dst_old=dst)
+    mn = oracle.rows("min", x, rows, length, accum=True, dst_old=dst)
+    assert mx.tolist() == [max(1.0, float(d)) for d in dst]
+    assert mn.tolist() == [min(1.0, float(d)) for d in dst]
+
+
+def test_rows_agree_with_full_per_row():
+    """Stride check: row r of the matrix reduces like the slice x[r]."""
+    rng = np.random.default_rng(14)
+    rows, length = 9, 23
+    x = _grid_uniform(rng, rows * length).reshape(rows, length)
+    s, _ = oracle.rows("sum", x, rows, length)
+    mx = oracle.rows("max", x, rows, length)
+    for r in range(rows):
+        assert s[r] == oracle.full_sum(x[r])[0]
+        assert mx[r] == oracle.full_max(x[r])
+
+
+def test_rows_len0():
+    x = np.zeros((4, 0), np.float32)
+    s, _ = oracle.rows("sum", x, 4, 0)
+    assert (s == 0).all()
+    dst = np.array([1.0, -2.0, 3.0, 0.5], np.float32)
+    s, _ = oracle.rows("sum", x, 4, 0, accum=True, dst_old=dst)
+    assert (s == dst).all()
+    with pytest.raises(oracle.OracleError):
+        oracle.rows("max", x, 4, 0)
+
+
+# ------------------------------------------------------------ ragged rows
+
+def test_ragged_matches_dense_layout():
+    rng = np.random.default_rng(15)
+    rows, length = 11, 19
+    x = _grid_uniform(rng, rows * length)
+    off = np.arange(rows + 1, dtype=np.int64) * length
+    for op in ("max", "min"):
+        assert (oracle.ragged(op, x, off) == oracle.rows(op, x, rows, length)).all()
+    assert (oracle.ragged("sum", x, off)[0] == oracle.rows("sum", x, rows, length)[0]).all()
+
+
+def test_ragged_bruteforce_with_empty_rows():
+    """Lengths 0..40 (8..40 is the workload's range; 0 tests empty rows)."""
+    rng = np.random.default_rng(16)
+    lens = rng.integers(0, 41, size=200)
+    lens[::17] = 0
+    off = np.zeros(lens.size + 1, np.int64)
+    off[1:] = np.cumsum(lens)
+    x = _grid_uniform(rng, int(off[-1]), -4.0, 4.0)
+    dst = _grid_uniform(rng, lens.size, -1.0, 1.0)
+    for accum in (False, True):
+        s, ab = oracle.ragged("sum", x, off, accum, dst)
+        mx = oracle.ragged("max", x, off, accum, dst)
+        mn = oracle.ragged("min", x, off, accum, dst)
+        for r in range(lens.size):
+            row = [float(v) for v in x[off[r]:off[r + 1]]]
+            init = [float(dst[r])] if accum else []
+            assert s[r] == math.fsum(init + row)
+            assert ab[r] == math.fsum(abs(v) for v in init + row)
+            assert mx[r] == max(init + row, default=-math.inf)
+            assert mn[r] == min(init + row, default=math.inf)
+
+
+def test_ragged_rejects_decreasing_offsets():
+    x = np.ones(10, np.float32)
+    with pytest.raises(oracle.OracleError):
+        oracle.ragged("sum", x, np.array([0, 5, 3, 10], np.int64))
+    with pytest.raises(oracle.OracleError):
+        oracle.ragged("max", x, np.array([1, 5, 10], np.int64))
+
+
+# ------------------------------------------------------------ TCOLPROD f32
+
+def _f32_of(fr: Fraction) -> np.float32:
+    """Nearest float32 of an exact rational whose numerator and denominator
+    fit in 53 bits (so Fraction -> double is exact, then one rounding)."""
+    return np.float32(fr.numerator / fr.denominator)
+
+
+def test_tcolprod_16x16_page_example():
+    """pto-isa docs, "TCOLPROD", "Examples": 16 x 16 float tile -> 1 x 16,
+    with constant columns whose products have closed forms."""
+    lines = golden_lines("tcolprod_16x16.txt")
+    R = int(lines[0][1]); C = int(lines[1][1])
+    cs, exp = [], []
+    for j, c, frac in lines[2:]:
+        cs.append(np.float32(float(c)))
+        exp.append(Fraction(frac))
+    x = np.tile(np.array(cs, np.float32), (R, 1))
+    out, outd = oracle.colprod_f32(x, R, C, want_double=True)
+    for j in range(C):
+        assert out[j] == _f32_of(exp[j]), j
+        assert outd[j] == exp[j].numerator / exp[j].denominator, j
+
+
+@pytest.mark.parametrize("c,R", [(1.0, 100), (-1.0, 99), (-1.0, 100), (2.0, 100), (0.5, 120), (-2.0, 37)])
+def test_colprod_constant_columns(c, R):
+    C = 7
+    x = np.full((R, C), c, np.float32)
+    out = oracle.colprod_f32(x, R, C)
+    assert (out == np.float32(c ** R)).all()
+
+
+def test_colprod_not_transposed():
+    """x[i,j] = c_j * s_i with s_i = +-1: out[j] = c_j**R * prod(s); a product
+    taken along rows instead of columns gives a different answer."""
+    R, C = 5, 3
+    c = np.array([2.0, 0.5, -3.0], np.float32)
+    s = np.array([1, -1, -1, -1, 1], np.float32)
+    x = (s[:, None] * c[None, :]).astype(np.float32)
+    out = oracle.colprod_f32(x, R, C)
+    assert out.tolist() == [float(cj) ** R * -1.0 for cj in c]
+
+
+def test_colprod_bruteforce_exact():
+    rng = np.random.default_rng(17)
+    for R, C in [(1, 1), (1, 5), (3, 4), (8, 3), (13, 6), (40, 2)]:
+        x = rng.uniform(0.5, 1.5, size=(R, C)).astype(np.float32)
+        out, outd = oracle.colprod_f32(x, R, C, want_double=True)
+        for j in range(C):
+            ex = math.prod(Fraction(float(v)) for v in x[:, j])
+            rel = abs(Fraction(float(outd[j])) - ex) / ex
+            assert rel <= R * 2.0**-53
+            # one fp32 rounding of a value within R ulp(double) of exact
+            ref = np.float32(float(ex))
+            assert abs(int(out[j].view(np.int32)) - int(ref.view(np.int32))) <= 1
+
+
+def test_colprod_early_return_leaves_dst():
+    """pto-isa docs, "TCOLPROD", "Constraints": R == 0 or C == 0 returns early."""
+    sentinel = np.full(4, 7.25, np.float32)
+    oracle.colprod_f32(np.zeros((0, 4), np.float32), 0, 4, out_f=sentinel)
+    assert (sentinel == 7.25).all()
+    oracle.colprod_f32(np.zeros((3, 0), np.float32), 3, 0, out_f=sentinel)
+    assert (sentinel == 7.25).all()
+    isent = np.full(4, -9, np.int32)
+    oracle.colprod_i32(np.zeros((0, 4), np.int32), 0, 4, out=isent)
+    assert (isent == -9).all()
+
+
+# ------------------------------------------------------------ TCOLPROD i32
+
+def test_colprod_i32_wrap_closed_forms():
+    for c, R, expected in golden_lines("tcolprod_i32_wrap.txt"):
+        c, R, expected = int(c), int(R), int(expected)
+        x = np.full((R, 3), c, np.int32)
+        out = oracle.colprod_i32(x, R, 3)
+        assert (out == expected).all(), (c, R)
+
+
+def _wrap32(v: int) -> int:
+    v %= 1 << 32
+    return v - (1 << 32) if v >= 1 << 31 else v
+
+
+def test_colprod_i32_bruteforce_bigint():
+    rng = np.random.default_rng(18)
+    for R, C in [(1, 4), (7, 5), (33, 3), (64, 9), (100, 2)]:
+        x = rng.choice(np.array([-3, -2, -1, 1, 2, 3], np.int32), size=(R, C))
+        out = oracle.colprod_i32(x, R, C)
+        for j in range(C):
+            assert out[j] == _wrap32(math.prod(int(v) for v in x[:, j]))
+
+
+def test_colprod_i32_large_values_wrap():
+    rng = np.random.default_rng(19)
+    R, C = 9, 6
+    x = rng.integers(-2**31, 2**31, size=(R, C), dtype=np.int64).astype(np.int32)
+    out = oracle.colprod_i32(x, R, C)
+    for j in range(C):
+        assert out[j] == _wrap32(math.prod(int(v) for v in x[:, j]))

@@ -1,0 +1,503 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 axis reductions.
+
+One step = one pass of every reduction over the five synthetic workloads:
+
+  full    2**20 fp32 U[-1,1)               sum, max, min
+  rows    65536 x 1024 fp32 N(0,1)         sum, max, min, sum with accum
+  full    2**30 fp32 N(0,1) (4 GiB)        sum, max, min
+  colprod 4096 x 16384 fp32 U[.999,1.001]  and 64 x 65536 int32 {+-1,+-2,+-3}
+  ragged  2**22 rows of 8..40 fp32 U[-4,4) sum, max, min
+
+The ops run interleaved (every buffer is re-read only after at least 4 GiB of
+other reads, so each op sees cold L2).  ``value`` is the algorithmic bytes of
+a step (each input read once, each output written once) over the device time
+of the step, in GB/s, summed over ranks (weak scaling: every rank runs the
+whole workload on its own GPU).  Per-op times, the roofline of the dominant
+kernel (the 4 GiB full reduction), an end-to-end figure through host buffers,
+the grid-stage comparison of the full reduction, and the CPU oracle timed on
+a sample of the same workload go into the same JSON line.
+
+``--impl reference`` times the CPU oracle alone on the host (no GPU), one
+bounded sample of the workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s (and % of ~8 TB/s) for full/row sum-max-min and col-prod"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = ("all five reduction workloads, one pass of every op: full 2^20 + full 2^30 (sum/max/min), "
+            "rows 65536x1024 (sum/max/min + sum accum), colprod f32 4096x16384 + i32 64x65536, "
+            "ragged 2^22 rows of 8..40 (sum/max/min)")
+DOMINANT = "seg_kernel (red_full, 2^30 fp32 sum/max/min)"
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "int_tensor_reductions_gb300", "csrc", f)
+                  for f in ("red_full.cu", "red_prims.cuh")]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-stage-compare", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def sha_of(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return None
+
+
+def traffic_per_launch():
+    """DRAM bytes per launch of the dominant kernel from the last ncu capture,
+    or None when none was taken of the kernel as it is now."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if t.get("sources_sha256") != sha_of(KERNEL_SOURCES):
+        return None
+    return t.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.window = None
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.monotonic(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for t, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 8:
+                continue
+            try:
+                rows.append((t, float(parts[0]), float(parts[1]), parts[4:]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        t0, t1 = self.window or (rows[0][0], rows[-1][0])
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05] or \
+            [min(rows, key=lambda r: abs(r[0] - (t0 + t1) / 2))]
+        reasons = sorted({name for r in inside for name, v in zip(self.NAMES, r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ------------------------------------------------------------ the workload
+
+class Workload:
+    """Device inputs and outputs of one step and the ops in step order."""
+
+    def __init__(self, device, frac=1.0, host_only=False):
+        import torch
+        from int_tensor_reductions_gb300 import synth
+        self.torch = torch
+        gen_dev = "cpu" if host_only else device
+        f = frac
+
+        def n_of(n):
+            return max(8, int(n * f))
+
+        self.x1 = synth.cfg1(gen_dev, n=n_of(synth.CFG1_N))
+        self.x2, self.dst2 = synth.cfg2(gen_dev, rows=n_of(synth.CFG2_ROWS), length=synth.CFG2_LEN)
+        self.x3 = synth.cfg3(gen_dev, n=n_of(synth.CFG3_N))
+        self.x4a = synth.cfg4a(gen_dev, R=n_of(synth.CFG4A_R), C=synth.CFG4A_C)
+        self.x4b = synth.cfg4b(gen_dev, R=max(1, int(synth.CFG4B_R * f)), C=synth.CFG4B_C)
+        self.x5, self.off5 = synth.cfg5(gen_dev, rows=n_of(synth.CFG5_ROWS))
+        self.inputs = [self.x1, self.x2, self.dst2, self.x3, self.x4a, self.x4b, self.x5, self.off5]
+        r2, l2 = self.x2.shape
+        n5 = self.off5.numel() - 1
+        nnz5 = self.x5.numel()
+        self.bytes_of = {
+            "full1": 4 * self.x1.numel() + 4,
+            "full3": 4 * self.x3.numel() + 4,
+            "rows2": 4 * r2 * l2 + 4 * r2,
+            "rows2_accum": 4 * r2 * l2 + 8 * r2,
+            "colprod4a": 4 * self.x4a.numel() + 4 * self.x4a.shape[1],
+            "colprod4b": 4 * self.x4b.numel() + 4 * self.x4b.shape[1],
+            "ragged5": 4 * nnz5 + 8 * (n5 + 1) + 4 * n5,
+        }
+        # step order: interleaved so that no buffer is re-read while hot
+        self.plan = [
+            ("full1 sum", "full1"), ("full3 sum", "full3"), ("rows2 sum", "rows2"), ("ragged5 sum", "ragged5"),
+            ("colprod4a f32", "colprod4a"),
+            ("full1 max", "full1"), ("full3 max", "full3"), ("rows2 max", "rows2"), ("ragged5 max", "ragged5"),
+            ("colprod4b i32", "colprod4b"),
+            ("full1 min", "full1"), ("full3 min", "full3"), ("rows2 min", "rows2"), ("ragged5 min", "ragged5"),
+            ("rows2 sum accum", "rows2_accum"),
+        ]
+        self.step_bytes = sum(self.bytes_of[k] for _, k in self.plan)
+        if not host_only:
+            t = torch
+            self.o1 = {op: t.empty(1, device=device) for op in ("sum", "max", "min")}
+            self.o3 = {op: t.empty(1, device=device) for op in ("sum", "max", "min")}
+            self.o2 = {op: t.empty(r2, device=device) for op in ("sum", "max", "min")}
+            self.o2acc = self.dst2.clone()
+            self.o4a = t.empty(self.x4a.shape[1], device=device)
+            self.o4b = t.empty(self.x4b.shape[1], dtype=t.int32, device=device)
+            self.o5 = {op: t.empty(n5, device=device) for op in ("sum", "max", "min")}
+            self.outputs = list(self.o1.values()) + list(self.o3.values()) + list(self.o2.values()) + \
+                [self.o2acc, self.o4a, self.o4b] + list(self.o5.values())
+
+    def gpu_call(self, name):
+        import int_tensor_reductions_gb300 as itr
+        kind, op = name.split(" ")[0], name.split(" ")[1]
+        if kind == "full1":
+            return lambda: itr.red_full(op, self.x1, self.o1[op])
+        if kind == "full3":
+            return lambda: itr.red_full(op, self.x3, self.o3[op])
+        if kind == "rows2" and name.endswith("accum"):
+            return lambda: itr.red_rows("sum", self.x2, accum=True, out=self.o2acc)
+        if kind == "rows2":
+            return lambda: itr.red_rows(op, self.x2, out=self.o2[op])
+        if kind == "ragged5":
+            return lambda: itr.red_rows_ragged(op, self.x5, self.off5, out=self.o5[op])
+        if kind == "colprod4a":
+            return lambda: itr.red_colprod(self.x4a, self.o4a)
+        if kind == "colprod4b":
+            return lambda: itr.red_colprod(self.x4b, self.o4b)
+        raise KeyError(name)
+
+
+def oracle_step(w: Workload, host):
+    """One pass of every op through the CPU oracle on host arrays; returns
+    the seconds spent inside the oracle calls."""
+    import oracle
+    x1, x2, dst2, x3, x4a, x4b, x5, off5 = host
+    r2, l2 = x2.shape
+    R4a, C4a = x4a.shape
+    R4b, C4b = x4b.shape
+    t = 0.0
+    for name, _ in w.plan:
+        kind, op = name.split(" ")[0], name.split(" ")[1]
+        t0 = time.perf_counter()
+        if kind == "full1":
+            oracle.full(op, x1)
+        elif kind == "full3":
+            oracle.full(op, x3)
+        elif kind == "rows2" and name.endswith("accum"):
+            oracle.rows("sum", x2, r2, l2, True, dst2)
+        elif kind == "rows2":
+            oracle.rows(op, x2, r2, l2)
+        elif kind == "ragged5":
+            oracle.ragged(op, x5, off5)
+        elif kind == "colprod4a":
+            oracle.colprod_f32(x4a, R4a, C4a)
+        else:
+            oracle.colprod_i32(x4b, R4b, C4b)
+        t += time.perf_counter() - t0
+    return t
+
+
+# ------------------------------------------------------------- reference
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import numpy as np  # noqa: F401
+    # Size each step's sample so that warm-up plus timed steps stay near
+    # two minutes of single-thread oracle time (calibrated on a small probe).
+    probe = Workload(None, frac=1.0 / 256, host_only=True)
+    host = [t.numpy() for t in probe.inputs]
+    t_probe = max(oracle_step(probe, host), 1e-6)
+    full_est = t_probe * 256
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    frac = min(1.0, max(1.0 / 256, budget / full_est))
+    w = Workload(None, frac=frac, host_only=True)
+    host = [t.numpy() for t in w.inputs]
+    for _ in range(args.warmup):
+        oracle_step(w, host)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(w, host)
+    dt = time.perf_counter() - t0
+    value = w.step_bytes * args.steps / dt / 1e9
+    sample = f"{frac:.4g} of every workload (leading rows / elements), {w.step_bytes} bytes per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32/i32",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ ours
+
+def run_ours(args):
+    import torch
+    import int_tensor_reductions_gb300 as itr
+    from int_tensor_reductions_gb300 import _build
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device; this library has no CPU path")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    _build.build_lib()
+    stream = torch.cuda.current_stream(dev)
+
+    w = Workload(dev)
+    calls = [(name, key, w.gpu_call(name)) for name, key in w.plan]
+    torch.cuda.synchronize()
+
+    def step():
+        for _, _, fn in calls:
+            fn()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    # per-op events across every timed step
+    K = args.steps
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
+          for _ in range(K)]
+    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gpu_index = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    if vis and vis.split(",")[0].strip().isdigit():
+        gpu_index = int(vis.split(",")[local].strip())
+    sampler = ClockSampler(gpu_index)
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = itr.red_launch_count()
+    h0 = time.monotonic()
+    t_begin.record(stream)
+    for k in range(K):
+        for i, (_, _, fn) in enumerate(calls):
+            ev[k][i][0].record(stream)
+            fn()
+            ev[k][i][1].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    h1 = time.monotonic()
+    if dist:
+        dist.barrier()
+    launches = itr.red_launch_count() - launches0
+    sampler.mark(h0, h1)
+    clocks = sampler.stop()
+    total_ms = t_begin.elapsed_time(t_end)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t[0])
+    per_op = {}
+    for i, (name, key, _) in enumerate(calls):
+        ms = [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(K)]
+        mean = sum(ms) / K
+        per_op[name] = {"ms": round(mean, 5), "gbs": round(w.bytes_of[key] / (mean * 1e-3) / 1e9, 1)}
+
+    value = world * w.step_bytes * K / (total_ms * 1e-3) / 1e9
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks and "hbm_gbs" in peaks else FALLBACK_HBM_GBS
+    peak_src = "measured" if peaks and "hbm_gbs" in peaks else "fallback"
+    dom = [per_op[n]["ms"] for n in ("full3 sum", "full3 max", "full3 min")]
+    dom_ms = sum(dom) / len(dom)
+    achieved = w.bytes_of["full3"] / (dom_ms * 1e-3) / 1e9
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32/i32", "data": "synthetic",
+        "config": {
+            "workload": WORKLOAD,
+            "bytes_per_step": w.step_bytes,
+            "l2": "inputs larger than L2 between reuses: ops interleaved so every buffer is re-read only "
+                  "after >= 4 GiB of other reads (L2 is 126 MiB)",
+            "full_grid_stage": {1: "two-pass", 2: "last-block", 3: "atomic"}[itr.red_get_full_mode()],
+            "parallelism": f"replicas x{world}",
+        },
+        "frac_of_nominal_8TBs": round(value / world / NOMINAL_HBM_GBS, 4),
+        "roofline": {
+            "bound": "hbm", "kernel": DOMINANT, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": peak_src,
+            "frac_of_nominal_8TBs": round(achieved / NOMINAL_HBM_GBS, 4),
+            "traffic": traffic_per_launch(), "algorithmic_bytes_per_launch": w.bytes_of["full3"],
+        },
+        "ops": per_op,
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+    }
+
+    if not args.no_stage_compare:
+        result["full_grid_stage_compare"] = compare_stages(w, stream)
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(w, calls, stream, args.e2e_steps, world, dist, dev)
+
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(w)
+
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def compare_stages(w, stream, reps=10):
+    """GB/s of the 4 GiB full reduction under each grid stage."""
+    import torch
+    import int_tensor_reductions_gb300 as itr
+    keep = itr.red_get_full_mode()
+    out = {}
+    for mode, label in ((itr.RED_MODE_TWO_PASS, "two-pass"), (itr.RED_MODE_LAST_BLOCK, "last-block"),
+                        (itr.RED_MODE_ATOMIC, "atomic")):
+        itr.red_set_full_mode(mode)
+        res = {}
+        for op in ("sum", "max", "min"):
+            for _ in range(2):
+                itr.red_full(op, w.x3, w.o3[op])
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(reps):
+                itr.red_full(op, w.x3, w.o3[op])
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            res[op] = round(w.bytes_of["full3"] / (ms * 1e-3) / 1e9, 1)
+        out[label] = res
+    itr.red_set_full_mode(keep)
+    return {"unit": "GB/s", "note": "2^30 fp32, back-to-back calls (4 GiB > L2)", **out}
+
+
+def run_e2e(w, calls, stream, steps, world, dist, dev):
+    """Same step through the public API from pinned host buffers: every step
+    copies its inputs host->device and its results device->host."""
+    import torch
+    host_in = [t.cpu().pin_memory() for t in w.inputs]
+    host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in w.outputs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+
+    def step():
+        for d, h in zip(w.inputs, host_in):
+            d.copy_(h, non_blocking=True)
+        for _, _, fn in calls:
+            fn()
+        for h, d in zip(host_out, w.outputs):
+            h.copy_(d, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t[0])
+    value = world * w.step_bytes * steps / (ms * 1e-3) / 1e9
+    return {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps, "ms_per_step": round(ms / steps, 3)}
+
+
+def cpu_baseline(w):
+    """The oracle, single-threaded, over one full pass of the same workload
+    (the same input bits, copied to the host)."""
+    host = [t.cpu().numpy() for t in w.inputs]
+    secs = oracle_step(w, host)
+    return {"value": round(w.step_bytes / secs / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "one full step (all 15 ops on the full-size inputs), single thread",
+            "seconds": round(secs, 2), "host_cpus": os.cpu_count()}
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

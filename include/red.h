@@ -1,0 +1,185 @@
+/*
+ * red.h -- C ABI of libred.so, a GB300 (sm_103a) library of fp32 / int32 axis
+ * reductions:
+ *
+ *   red_full         full-vector sum / max / min of fp32 data to one scalar;
+ *   red_rows         per-row sum / max / min of a dense row-major fp32 matrix,
+ *                    optionally folding the old destination value in (accum);
+ *   red_rows_ragged  the same for packed rows of varying length (CSR offsets);
+ *   red_colprod      TCOLPROD column products dst[0,j] = prod_i src[i,j] for
+ *                    fp32 and (wrapping) int32 matrices.
+ *
+ * Sources of the semantics (cited by page title and section):
+ *   [TVM] Apache TVM docs, "reduction -> sm100_packed": "Algorithm" (sum of a
+ *         1-D float32 vector through an 8-wide packed add.f32x2 fold; max / min
+ *         through a 4-wide max3 / min3 fold), "How inputs change the
+ *         algorithm" (accum folds the old dst value into the first
+ *         accumulator slot), "Demonstration program" (Tx.sum(dst, src,
+ *         accum), destination-passing, B == sum(A) for 32 elements).
+ *   [BLK] Triton vector-accumulation blog post (imxueqiu.com), the C version
+ *         of the block reduce: warp butterfly, shared-memory stage, one
+ *         atomic per block.
+ *   [PTO] pto-isa docs, "TCOLPROD": "Math Interpretation" (dst[0,j] =
+ *         prod_{i<R} src[i,j]), "Constraints" (row-major, same element type
+ *         for src and dst, early return when R == 0 or C == 0), "A2A3
+ *         implementation checks" (float and int32 among the element types).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers to data (x, offsets, out) are DEVICE pointers on the current
+ *     CUDA device, owned by the caller, which keeps them alive until the work
+ *     queued on `stream` has finished.  fp32 / int32 pointers must be 4-byte
+ *     aligned and int64 pointers 8-byte aligned; no larger alignment is needed
+ *     (the kernels peel an unaligned head and tail off each span).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and never synchronises the host.
+ *   - Status codes: RED_OK on success.  RED_EINVAL for bad arguments, detected
+ *     on the host before anything is launched (nothing is written then).
+ *     RED_ECUDA if a CUDA call or launch fails; RED_ENOMEM if the one-time
+ *     workspace allocation fails.  red_last_error() returns a message for the
+ *     last failing call of the calling thread.
+ *   - Workspace: partial results of the multi-CTA stages live in a workspace
+ *     that the library allocates once per device (16 MiB of partials plus
+ *     65536 counters, zeroed at allocation), on the first call that needs it.
+ *     That first call should therefore come before any CUDA stream capture.
+ *     The counters reset themselves at the end of every call, so calls on one
+ *     device must be ordered (one stream, or streams ordered by events):
+ *     two such calls running at the same time on one device race.
+ *   - fp32 sums use round-to-nearest with flush-to-zero packed adds and a
+ *     library-chosen summation order: the result equals the exact sum up to
+ *     rounding (tests bound it by 1e-5 * sum|x|).  Max / min are exact.
+ *     Integer products are exact modulo 2^32.
+ *   - NaN inputs are not supported (max / min then return an unspecified
+ *     operand); infinities propagate as in IEEE arithmetic.
+ */
+#ifndef RED_H
+#define RED_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as cudaStream_t. */
+typedef struct CUstream_st *red_stream_t;
+
+/* Reduction operator. */
+enum red_op { RED_SUM = 0, RED_MAX = 1, RED_MIN = 2 };
+
+/* Element type of red_colprod. */
+enum red_dtype { RED_F32 = 0, RED_I32 = 1 };
+
+/* Status codes. */
+enum red_status { RED_OK = 0, RED_EINVAL = -1, RED_ECUDA = -2, RED_ENOMEM = -3 };
+
+/* Grid stage of red_full (how the per-CTA partials become one scalar). */
+enum red_full_mode {
+    RED_MODE_AUTO = 0,       /* the measured default */
+    RED_MODE_TWO_PASS = 1,   /* partials to the workspace, then a second kernel */
+    RED_MODE_LAST_BLOCK = 2, /* one kernel; the last CTA to finish folds the partials */
+    RED_MODE_ATOMIC = 3      /* identity into *out, then one atomic per CTA */
+};
+
+/* Tuning knobs for measurement (0 restores the automatic choice). */
+enum red_knob {
+    RED_KNOB_ROWS_GROUP = 1,   /* lanes per dense row: 1, 2, 4, 8, 16 or 32 */
+    RED_KNOB_RAGGED_GROUP = 2, /* lanes per ragged row: 1, 2, 4, 8, 16 or 32 */
+    RED_KNOB_COLPROD_SPLITS = 3, /* CTAs along the row axis of red_colprod (>= 1) */
+    RED_KNOB_FULL_CTAS_PER_SM = 4 /* resident CTAs per SM for red_full (>= 1) */
+};
+
+/*
+ * red_full -- reduce a 1-D fp32 vector to one scalar.  [TVM] "Algorithm"
+ * (the thread-scope fold) applied per thread, then [BLK]'s warp butterfly and
+ * shared-memory stage per CTA, then the grid stage set by red_set_full_mode.
+ *   op     RED_SUM, RED_MAX or RED_MIN.
+ *   x      device pointer to n contiguous floats (may be NULL when n == 0).
+ *   n      number of elements, 0 <= n (n up to 2^40 is accepted).
+ *   out    device pointer to one float, written with the result.
+ *   stream CUDA stream the work is queued on.
+ * n == 0: RED_SUM writes 0; RED_MAX / RED_MIN return RED_EINVAL (an empty
+ * vector has no extreme).
+ */
+int red_full(int op, const float *x, int64_t n, float *out, red_stream_t stream);
+
+/*
+ * red_rows -- per-row reduction of a row-major fp32 matrix: row r is
+ * x[r*len .. r*len+len), out[r] = op over row r.  With accum != 0 the old
+ * value out[r] is folded in as one more operand ([TVM] "How inputs change the
+ * algorithm": accum folds the old dst value into the first accumulator slot).
+ *   op     RED_SUM, RED_MAX or RED_MIN.
+ *   x      device pointer to rows*len floats (leading dimension len).
+ *   rows   number of rows, >= 0; len row length, >= 0.
+ *   accum  0: overwrite out; non-zero: fold the old out[r] in.
+ *   out    device pointer to rows floats (read first when accum != 0).
+ * len == 0: RED_SUM writes zeros (accum: leaves out unchanged); RED_MAX /
+ * RED_MIN return RED_EINVAL.  rows == 0 does nothing.
+ */
+int red_rows(int op, const float *x, int64_t rows, int64_t len, int accum, float *out,
+             red_stream_t stream);
+
+/*
+ * red_rows_ragged -- per-row reduction of packed rows of varying length:
+ * row r is x[offsets[r] .. offsets[r+1]).  Same ops and accum as red_rows.
+ *   x        device pointer to nnz floats.
+ *   offsets  device pointer to rows+1 int64 values with offsets[0] = 0,
+ *            offsets non-decreasing and offsets[rows] = nnz.  The library
+ *            cannot check device-resident offsets without synchronising; it
+ *            clamps every offset to [0, nnz] (a decreasing pair reads as an
+ *            empty row), so it never reads outside x[0 .. nnz), but the
+ *            results of invalid offsets are unspecified.
+ *   rows     number of rows, >= 0.   nnz  number of values in x, >= 0.
+ *   out      device pointer to rows floats (read first when accum != 0).
+ * An empty row gives 0 for RED_SUM, -inf for RED_MAX and +inf for RED_MIN
+ * (the identity of the fold); with accum the old out[r] is kept.
+ */
+int red_rows_ragged(int op, const float *x, const int64_t *offsets, int64_t rows, int64_t nnz,
+                    int accum, float *out, red_stream_t stream);
+
+/*
+ * red_colprod -- [PTO] TCOLPROD: out[j] = prod_{i=0}^{R-1} x[i*C + j] for
+ * 0 <= j < C, x row-major R x C.
+ *   dtype  RED_F32 (fp32 products, round-to-nearest) or RED_I32 (int32
+ *          products wrapping modulo 2^32); x and out have this type.
+ *   x      device pointer to R*C elements.   out  device pointer to C elements.
+ *   R, C   >= 0.  R == 0 or C == 0 returns RED_OK at once and writes nothing
+ *          ([PTO] "Constraints": the implementation returns early).
+ */
+int red_colprod(int dtype, const void *x, int64_t R, int64_t C, void *out, red_stream_t stream);
+
+/* Select the grid stage of red_full (enum red_full_mode).  Process-wide.
+ * Returns RED_OK, or RED_EINVAL for an unknown mode. */
+int red_set_full_mode(int mode);
+
+/* The grid stage red_full uses now (never RED_MODE_AUTO: the resolved one). */
+int red_get_full_mode(void);
+
+/* Set a tuning knob (enum red_knob); value 0 restores the automatic choice.
+ * Returns RED_EINVAL for an unknown knob or an out-of-range value. */
+int red_set_knob(int knob, int value);
+
+/* Current value of a knob (0 = automatic), or RED_EINVAL for an unknown knob. */
+int red_get_knob(int knob);
+
+/* Message for the last non-OK status returned to the calling thread
+ * ("" if none).  The string is owned by the library and stays valid until
+ * the thread's next failing call. */
+const char *red_last_error(void);
+
+/* Free the calling thread's current device's workspace.  The caller must make
+ * sure no queued work still uses it (e.g. synchronise the device first); the
+ * next call that needs it allocates it again.  Returns RED_OK or RED_ECUDA. */
+int red_release_workspace(void);
+
+/* Number of kernels this library has launched in this process (all devices,
+ * all threads), for counting launches around a timed region. */
+uint64_t red_launch_count(void);
+
+/* ABI version of this header: 1. */
+int red_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RED_H */

@@ -1,0 +1,193 @@
+"""ctypes binding of libred.so: argument marshalling only."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+RED_SUM, RED_MAX, RED_MIN = 0, 1, 2
+RED_F32, RED_I32 = 0, 1
+RED_OK, RED_EINVAL, RED_ECUDA, RED_ENOMEM = 0, -1, -2, -3
+RED_MODE_AUTO, RED_MODE_TWO_PASS, RED_MODE_LAST_BLOCK, RED_MODE_ATOMIC = 0, 1, 2, 3
+RED_KNOB_ROWS_GROUP, RED_KNOB_RAGGED_GROUP, RED_KNOB_COLPROD_SPLITS, RED_KNOB_FULL_CTAS_PER_SM = 1, 2, 3, 4
+
+_OPS = {"sum": RED_SUM, "max": RED_MAX, "min": RED_MIN}
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libred.so")
+_lib = None
+
+_i64, _int, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+_SIGNATURES = {
+    "red_full": ([_int, _vp, _i64, _vp, _vp], _int),
+    "red_rows": ([_int, _vp, _i64, _i64, _int, _vp, _vp], _int),
+    "red_rows_ragged": ([_int, _vp, _vp, _i64, _i64, _int, _vp, _vp], _int),
+    "red_colprod": ([_int, _vp, _i64, _i64, _vp, _vp], _int),
+    "red_set_full_mode": ([_int], _int),
+    "red_get_full_mode": ([], _int),
+    "red_set_knob": ([_int, _int], _int),
+    "red_get_knob": ([_int], _int),
+    "red_last_error": ([], ctypes.c_char_p),
+    "red_release_workspace": ([], _int),
+    "red_launch_count": ([], ctypes.c_uint64),
+    "red_version": ([], _int),
+}
+
+
+class RedError(RuntimeError):
+    """A libred call returned a non-OK status."""
+
+    def __init__(self, status, message):
+        super().__init__(f"libred status {status}: {message}")
+        self.status = status
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded libred.so (ctypes.CDLL).  Raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it with int_tensor_reductions_gb300._build.build_lib() "
+                "(or __graft_entry__.build()); there is no fallback implementation")
+        l = ctypes.CDLL(_LIB_PATH)
+        for name, (args, res) in _SIGNATURES.items():
+            fn = getattr(l, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = l
+    return _lib
+
+
+def red_last_error() -> str:
+    return lib().red_last_error().decode()
+
+
+def _check(status):
+    if status != RED_OK:
+        raise RedError(status, red_last_error())
+
+
+def _op(op) -> int:
+    if isinstance(op, str):
+        return _OPS[op]
+    return int(op)
+
+
+def _stream(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need(t: torch.Tensor, name: str, dtypes):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name} must have dtype {dtypes}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def red_full(op, x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Reduce all of fp32 ``x`` to ``out`` (shape (1,)) on ``stream``."""
+    _need(x, "x", (torch.float32,))
+    if out is None:
+        out = torch.empty(1, dtype=torch.float32, device=x.device)
+    _need(out, "out", (torch.float32,))
+    with torch.cuda.device(x.device):
+        _check(lib().red_full(_op(op), x.data_ptr(), x.numel(), out.data_ptr(), _stream(stream, x.device)))
+    return out
+
+
+def red_rows(op, x: torch.Tensor, accum: bool = False, out: torch.Tensor | None = None,
+             stream=None) -> torch.Tensor:
+    """Per-row reduction of a (rows, len) row-major fp32 matrix into ``out[rows]``."""
+    _need(x, "x", (torch.float32,))
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D (rows, len)")
+    rows, length = x.shape
+    if out is None:
+        if accum:
+            raise ValueError("accum needs an existing out")
+        out = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _need(out, "out", (torch.float32,))
+    if out.numel() != rows:
+        raise ValueError("out must have one element per row")
+    with torch.cuda.device(x.device):
+        _check(lib().red_rows(_op(op), x.data_ptr(), rows, length, int(bool(accum)), out.data_ptr(),
+                              _stream(stream, x.device)))
+    return out
+
+
+def red_rows_ragged(op, x: torch.Tensor, offsets: torch.Tensor, accum: bool = False,
+                    out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Per-row reduction of packed rows x[offsets[r]:offsets[r+1]]."""
+    _need(x, "x", (torch.float32,))
+    _need(offsets, "offsets", (torch.int64,))
+    rows = offsets.numel() - 1
+    if rows < 0:
+        raise ValueError("offsets needs rows + 1 entries")
+    if out is None:
+        if accum:
+            raise ValueError("accum needs an existing out")
+        out = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _need(out, "out", (torch.float32,))
+    if out.numel() != rows:
+        raise ValueError("out must have one element per row")
+    with torch.cuda.device(x.device):
+        _check(lib().red_rows_ragged(_op(op), x.data_ptr(), offsets.data_ptr(), rows, x.numel(),
+                                     int(bool(accum)), out.data_ptr(), _stream(stream, x.device)))
+    return out
+
+
+def red_colprod(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """TCOLPROD: out[j] = prod_i x[i, j] for a (R, C) fp32 or int32 matrix."""
+    _need(x, "x", (torch.float32, torch.int32))
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D (R, C)")
+    R, C = x.shape
+    if out is None:
+        out = torch.empty(C, dtype=x.dtype, device=x.device)
+    _need(out, "out", (x.dtype,))
+    if out.numel() != C:
+        raise ValueError("out must have C elements")
+    dtype = RED_F32 if x.dtype == torch.float32 else RED_I32
+    with torch.cuda.device(x.device):
+        _check(lib().red_colprod(dtype, x.data_ptr(), R, C, out.data_ptr(), _stream(stream, x.device)))
+    return out
+
+
+def red_set_full_mode(mode: int) -> None:
+    _check(lib().red_set_full_mode(int(mode)))
+
+
+def red_get_full_mode() -> int:
+    return lib().red_get_full_mode()
+
+
+def red_set_knob(k: int, value: int) -> None:
+    _check(lib().red_set_knob(int(k), int(value)))
+
+
+def red_get_knob(k: int) -> int:
+    v = lib().red_get_knob(int(k))
+    if v < 0:
+        raise RedError(v, red_last_error())
+    return v
+
+
+def red_release_workspace() -> None:
+    _check(lib().red_release_workspace())
+
+
+def red_launch_count() -> int:
+    return int(lib().red_launch_count())
+
+
+def red_version() -> int:
+    return lib().red_version()

@@ -1,0 +1,283 @@
+// red_api.cu -- the extern "C" entry points of libred.so (declared and
+// documented in red.h): host-side argument checks before any launch, the
+// per-device workspace, error messages and tuning knobs.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "red.h"
+#include "red_internal.h"
+
+namespace red {
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+constexpr int64_t MAX_ELEMS = int64_t(1) << 44;  // guards index arithmetic
+
+thread_local char g_err[512] = "";
+std::mutex g_mu;
+Workspace g_ws[MAX_DEVICES];
+int g_sms[MAX_DEVICES];
+
+std::atomic<int> g_full_mode{RED_MODE_AUTO};
+std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_knobs[8];
+
+// Grid stage used when the mode is RED_MODE_AUTO.
+constexpr int AUTO_FULL_STAGE = RED_MODE_LAST_BLOCK;
+
+bool misaligned(const void *p, uintptr_t a) { return ((uintptr_t)p) % a != 0; }
+
+}  // namespace
+
+int fail(int code, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char *where)
+{
+    if (e == cudaSuccess)
+        return RED_OK;
+    return fail(RED_ECUDA, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+int device_info(DeviceInfo *info)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= MAX_DEVICES)
+        return fail(RED_ECUDA, "device ordinal %d out of range", dev);
+    if (g_sms[dev] == 0) {
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        g_sms[dev] = sms;
+    }
+    info->dev = dev;
+    info->sms = g_sms[dev];
+    return RED_OK;
+}
+
+int get_workspace(Workspace *ws)
+{
+    DeviceInfo di;
+    int st = device_info(&di);
+    if (st != RED_OK)
+        return st;
+    std::lock_guard<std::mutex> lock(g_mu);
+    Workspace &w = g_ws[di.dev];
+    if (!w.part) {
+        void *part = nullptr, *tick = nullptr;
+        cudaError_t e = cudaMalloc(&part, WS_PART_BYTES);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(RED_ENOMEM, "workspace allocation: %s", cudaGetErrorString(e));
+        }
+        e = cudaMalloc(&tick, WS_TICKETS * sizeof(unsigned));
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            cudaFree(part);
+            return fail(RED_ENOMEM, "workspace allocation: %s", cudaGetErrorString(e));
+        }
+        e = cudaMemset(tick, 0, WS_TICKETS * sizeof(unsigned));
+        if (e == cudaSuccess)
+            e = cudaDeviceSynchronize();
+        if (e != cudaSuccess) {
+            cudaFree(part);
+            cudaFree(tick);
+            return cuda_fail(e, "workspace initialisation");
+        }
+        w.part = part;
+        w.tick = static_cast<unsigned *>(tick);
+    }
+    *ws = w;
+    return RED_OK;
+}
+
+int knob(int which)
+{
+    if (which <= 0 || which >= 8)
+        return 0;
+    return g_knobs[which].load(std::memory_order_relaxed);
+}
+
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+int full_mode()
+{
+    const int m = g_full_mode.load(std::memory_order_relaxed);
+    return m == RED_MODE_AUTO ? AUTO_FULL_STAGE : m;
+}
+
+int occupancy(const void *kernel, int threads)
+{
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+}  // namespace red
+
+using namespace red;
+
+extern "C" {
+
+int red_full(int op, const float *x, int64_t n, float *out, red_stream_t stream)
+{
+    if (op < RED_SUM || op > RED_MIN)
+        return fail(RED_EINVAL, "red_full: unknown op %d", op);
+    if (n < 0 || n > MAX_ELEMS)
+        return fail(RED_EINVAL, "red_full: n = %lld out of range", (long long)n);
+    if (!out || misaligned(out, 4))
+        return fail(RED_EINVAL, "red_full: out is NULL or not 4-byte aligned");
+    if (n > 0 && (!x || misaligned(x, 4)))
+        return fail(RED_EINVAL, "red_full: x is NULL or not 4-byte aligned");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (n == 0) {
+        if (op != RED_SUM)
+            return fail(RED_EINVAL, "red_full: max/min of an empty vector");
+        return cuda_fail(cudaMemsetAsync(out, 0, sizeof(float), s), "red_full: cudaMemsetAsync");
+    }
+    return launch_full(op, x, n, out, s);
+}
+
+int red_rows(int op, const float *x, int64_t rows, int64_t len, int accum, float *out, red_stream_t stream)
+{
+    if (op < RED_SUM || op > RED_MIN)
+        return fail(RED_EINVAL, "red_rows: unknown op %d", op);
+    if (rows < 0 || len < 0 || rows > MAX_ELEMS || len > MAX_ELEMS ||
+        (len > 0 && rows > MAX_ELEMS / len))
+        return fail(RED_EINVAL, "red_rows: rows = %lld, len = %lld out of range", (long long)rows,
+                    (long long)len);
+    if (rows == 0)
+        return RED_OK;
+    if (!out || misaligned(out, 4))
+        return fail(RED_EINVAL, "red_rows: out is NULL or not 4-byte aligned");
+    if (len > 0 && (!x || misaligned(x, 4)))
+        return fail(RED_EINVAL, "red_rows: x is NULL or not 4-byte aligned");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (len == 0) {
+        if (op != RED_SUM)
+            return fail(RED_EINVAL, "red_rows: max/min of empty rows");
+        if (accum)
+            return RED_OK;
+        return cuda_fail(cudaMemsetAsync(out, 0, (size_t)rows * sizeof(float), s),
+                         "red_rows: cudaMemsetAsync");
+    }
+    return launch_rows(op, x, rows, len, accum ? 1 : 0, out, s);
+}
+
+int red_rows_ragged(int op, const float *x, const int64_t *offsets, int64_t rows, int64_t nnz, int accum,
+                    float *out, red_stream_t stream)
+{
+    if (op < RED_SUM || op > RED_MIN)
+        return fail(RED_EINVAL, "red_rows_ragged: unknown op %d", op);
+    if (rows < 0 || nnz < 0 || rows > MAX_ELEMS || nnz > MAX_ELEMS)
+        return fail(RED_EINVAL, "red_rows_ragged: rows = %lld, nnz = %lld out of range", (long long)rows,
+                    (long long)nnz);
+    if (rows == 0)
+        return RED_OK;
+    if (!offsets || misaligned(offsets, 8))
+        return fail(RED_EINVAL, "red_rows_ragged: offsets is NULL or not 8-byte aligned");
+    if (!out || misaligned(out, 4))
+        return fail(RED_EINVAL, "red_rows_ragged: out is NULL or not 4-byte aligned");
+    if (nnz > 0 && (!x || misaligned(x, 4)))
+        return fail(RED_EINVAL, "red_rows_ragged: x is NULL or not 4-byte aligned");
+    return launch_ragged(op, x, offsets, rows, nnz, accum ? 1 : 0, out,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+int red_colprod(int dtype, const void *x, int64_t R, int64_t C, void *out, red_stream_t stream)
+{
+    if (dtype != RED_F32 && dtype != RED_I32)
+        return fail(RED_EINVAL, "red_colprod: unknown dtype %d", dtype);
+    if (R < 0 || C < 0 || R > MAX_ELEMS || C > MAX_ELEMS || (C > 0 && R > MAX_ELEMS / C))
+        return fail(RED_EINVAL, "red_colprod: R = %lld, C = %lld out of range", (long long)R, (long long)C);
+    if (R == 0 || C == 0)
+        return RED_OK;  // TCOLPROD returns early on an empty tile; dst untouched
+    if (!x || misaligned(x, 4))
+        return fail(RED_EINVAL, "red_colprod: x is NULL or not 4-byte aligned");
+    if (!out || misaligned(out, 4))
+        return fail(RED_EINVAL, "red_colprod: out is NULL or not 4-byte aligned");
+    return launch_colprod(dtype, x, R, C, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int red_set_full_mode(int mode)
+{
+    if (mode < RED_MODE_AUTO || mode > RED_MODE_ATOMIC)
+        return fail(RED_EINVAL, "red_set_full_mode: unknown mode %d", mode);
+    g_full_mode.store(mode, std::memory_order_relaxed);
+    return RED_OK;
+}
+
+int red_get_full_mode(void) { return full_mode(); }
+
+int red_set_knob(int k, int value)
+{
+    switch (k) {
+    case RED_KNOB_ROWS_GROUP:
+    case RED_KNOB_RAGGED_GROUP:
+        if (!(value == 0 || value == 1 || value == 2 || value == 4 || value == 8 || value == 16 || value == 32))
+            return fail(RED_EINVAL, "red_set_knob: lanes per row must be 0 or a power of two <= 32");
+        break;
+    case RED_KNOB_COLPROD_SPLITS:
+        if (value < 0 || value > 65535)
+            return fail(RED_EINVAL, "red_set_knob: colprod splits must be in 0..65535");
+        break;
+    case RED_KNOB_FULL_CTAS_PER_SM:
+        if (value < 0 || value > 32)
+            return fail(RED_EINVAL, "red_set_knob: CTAs per SM must be in 0..32");
+        break;
+    default:
+        return fail(RED_EINVAL, "red_set_knob: unknown knob %d", k);
+    }
+    g_knobs[k].store(value, std::memory_order_relaxed);
+    return RED_OK;
+}
+
+int red_get_knob(int k)
+{
+    if (k < RED_KNOB_ROWS_GROUP || k > RED_KNOB_FULL_CTAS_PER_SM)
+        return fail(RED_EINVAL, "red_get_knob: unknown knob %d", k);
+    return knob(k);
+}
+
+const char *red_last_error(void) { return g_err; }
+
+int red_release_workspace(void)
+{
+    DeviceInfo di;
+    const int st = device_info(&di);
+    if (st != RED_OK)
+        return st;
+    std::lock_guard<std::mutex> lock(g_mu);
+    Workspace &w = g_ws[di.dev];
+    cudaError_t e = cudaSuccess, e2 = cudaSuccess;
+    if (w.part)
+        e = cudaFree(w.part);
+    if (w.tick)
+        e2 = cudaFree(w.tick);
+    w.part = nullptr;
+    w.tick = nullptr;
+    if (e != cudaSuccess)
+        return cuda_fail(e, "red_release_workspace");
+    return cuda_fail(e2, "red_release_workspace");
+}
+
+uint64_t red_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int red_version(void) { return 1; }
+
+}  // extern "C"

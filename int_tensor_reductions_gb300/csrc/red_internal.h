@@ -1,0 +1,54 @@
+// red_internal.h -- host-side plumbing shared by the library's translation
+// units: device facts, the per-device workspace, error reporting, knobs and
+// the kernel launchers behind the C entry points.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace red {
+
+// Workspace held once per device: fp32/uint32 partials of the multi-CTA
+// stages and the arrival counters of the last-block stages.
+constexpr size_t WS_PART_BYTES = size_t(16) << 20;        // 16 MiB
+constexpr size_t WS_PART_ELEMS = WS_PART_BYTES / 4;       // 4 Mi 32-bit words
+constexpr int WS_TICKETS = 65536;
+
+struct Workspace {
+    void *part = nullptr;        // WS_PART_BYTES bytes
+    unsigned *tick = nullptr;    // WS_TICKETS counters, zero between calls
+};
+
+struct DeviceInfo {
+    int dev = 0;
+    int sms = 0;
+};
+
+// Status helpers (codes of red.h).  fail() records a printf-style message
+// for red_last_error() and returns `code`.
+int fail(int code, const char *fmt, ...);
+int cuda_fail(cudaError_t e, const char *where);
+
+int device_info(DeviceInfo *info);
+int get_workspace(Workspace *ws);
+
+int knob(int which);        // 0 = automatic
+void count_launches(int n); // adds n to red_launch_count()
+int full_mode();            // resolved grid stage of red_full (1, 2 or 3)
+
+// Launchers: arguments have been validated by the entry points.
+int launch_full(int op, const float *x, int64_t n, float *out, cudaStream_t s);
+int launch_rows_split(int op, const float *x, int64_t rows, int64_t len, int accum, float *out,
+                      cudaStream_t s, const DeviceInfo &di);
+int launch_rows(int op, const float *x, int64_t rows, int64_t len, int accum, float *out,
+                cudaStream_t s);
+int launch_ragged(int op, const float *x, const int64_t *off, int64_t rows, int64_t nnz, int accum,
+                  float *out, cudaStream_t s);
+int launch_colprod(int dtype, const void *x, int64_t R, int64_t C, void *out, cudaStream_t s);
+
+// Resident CTAs per SM of a kernel at `threads` threads and no dynamic shared
+// memory (cached by the callers).
+int occupancy(const void *kernel, int threads);
+
+}  // namespace red

@@ -1,0 +1,232 @@
+// red_prims.cuh -- device building blocks of the reduction kernels (sm_103a).
+//
+// * Packed pairwise fp32 add, round-to-nearest, flush-to-zero: the
+//   add.rn.ftz.f32x2 instruction of Blackwell, two float lanes per
+//   instruction (Apache TVM docs, "reduction -> sm100_packed", sections
+//   "Algorithm" and "Generated CUDA").
+// * 3-input max / min (the max3 / min3 fold of the same page, "Algorithm":
+//   a 4-wide accumulator folded three values at a time), written as the
+//   three-operand max.f32 / min.f32 forms.
+// * The per-thread fold: an 8-wide sum accumulator fed by chunks of 8
+//   (four packed adds per chunk), the scalar remainder, and the final
+//   8 -> 4 -> 2 -> 1 collapse; a 4-wide max / min accumulator.
+// * Warp butterfly (__shfl_xor_sync) and the shared-memory CTA stage of the
+//   block reduce in the Triton vector-accumulation blog post (imxueqiu.com),
+//   C version: warp tree, lane 0 of each warp to shared memory, barrier,
+//   second warp tree.
+// * Streaming vector loads: 256-bit (8 x fp32) and 128-bit, read-only path,
+//   no L1 allocation (every byte is read once).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace red {
+
+enum : int { OP_SUM = 0, OP_MAX = 1, OP_MIN = 2 };
+
+// ------------------------------------------------------------ packed math
+
+__device__ __forceinline__ float2 add_f32x2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\t"
+        "mov.b64 pb, {%4, %5};\n\t"
+        "add.rn.ftz.f32x2 pd, pa, pb;\n\t"
+        "mov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float max3f(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ float min3f(float a, float b, float c)
+{
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+__device__ __forceinline__ float add_ftz(float a, float b)
+{
+    float d;
+    asm("add.rn.ftz.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+// --------------------------------------------------------------- loads
+
+// 8 consecutive floats from a 32-byte aligned address.
+__device__ __forceinline__ void ld8(const float *p, float (&v)[8])
+{
+    asm volatile("ld.global.nc.L1::no_allocate.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]),
+                   "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
+                 : "l"(p));
+}
+
+// 8 consecutive 32-bit words from a 32-byte aligned address.
+__device__ __forceinline__ void ld8u(const uint32_t *p, uint32_t (&v)[8])
+{
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]),
+                   "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                 : "l"(p));
+}
+
+// 4 consecutive 32-bit words from a 16-byte aligned address.
+__device__ __forceinline__ void ld4u(const uint32_t *p, uint32_t (&v)[4])
+{
+    asm volatile("ld.global.nc.L1::no_allocate.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+                 : "l"(p));
+}
+
+__device__ __forceinline__ float ld1(const float *p) { return __ldg(p); }
+
+// ------------------------------------------------------ operator traits
+
+template <int OP>
+struct Op;
+
+template <>
+struct Op<OP_SUM> {
+    static __device__ __forceinline__ float identity() { return 0.0f; }
+    static __device__ __forceinline__ float combine(float a, float b) { return add_ftz(a, b); }
+};
+
+template <>
+struct Op<OP_MAX> {
+    static __device__ __forceinline__ float identity() { return __int_as_float(0xff800000); }
+    static __device__ __forceinline__ float combine(float a, float b) { return fmaxf(a, b); }
+};
+
+template <>
+struct Op<OP_MIN> {
+    static __device__ __forceinline__ float identity() { return __int_as_float(0x7f800000); }
+    static __device__ __forceinline__ float combine(float a, float b) { return fminf(a, b); }
+};
+
+// ------------------------------------------------------ per-thread fold
+
+template <int OP>
+struct Fold;
+
+// 8-wide fp32 accumulator.  chunk(): four packed adds fold 8 new values in;
+// scalar(): remainder (and accum) values go into slot 0; finish(): the
+// 8 -> 4 -> 2 -> 1 collapse with three packed adds and one scalar add.
+template <>
+struct Fold<OP_SUM> {
+    float2 a[4];
+    __device__ __forceinline__ void init()
+    {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            a[k] = make_float2(0.0f, 0.0f);
+    }
+    __device__ __forceinline__ void chunk(const float (&v)[8])
+    {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            a[k] = add_f32x2(a[k], make_float2(v[2 * k], v[2 * k + 1]));
+    }
+    __device__ __forceinline__ void scalar(float v) { a[0].x = add_ftz(a[0].x, v); }
+    __device__ __forceinline__ float finish() const
+    {
+        float2 s01 = add_f32x2(a[0], a[1]);  // (0,1) + (2,3)
+        float2 s45 = add_f32x2(a[2], a[3]);  // (4,5) + (6,7)
+        float2 s = add_f32x2(s01, s45);
+        return add_ftz(s.x, s.y);
+    }
+};
+
+// 4-wide accumulator; each max3 folds one slot with two new values.
+template <>
+struct Fold<OP_MAX> {
+    float m[4];
+    __device__ __forceinline__ void init()
+    {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            m[k] = Op<OP_MAX>::identity();
+    }
+    __device__ __forceinline__ void chunk(const float (&v)[8])
+    {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            m[k] = max3f(m[k], v[2 * k], v[2 * k + 1]);
+    }
+    __device__ __forceinline__ void scalar(float v) { m[0] = fmaxf(m[0], v); }
+    __device__ __forceinline__ float finish() const { return fmaxf(max3f(m[0], m[1], m[2]), m[3]); }
+};
+
+template <>
+struct Fold<OP_MIN> {
+    float m[4];
+    __device__ __forceinline__ void init()
+    {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            m[k] = Op<OP_MIN>::identity();
+    }
+    __device__ __forceinline__ void chunk(const float (&v)[8])
+    {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            m[k] = min3f(m[k], v[2 * k], v[2 * k + 1]);
+    }
+    __device__ __forceinline__ void scalar(float v) { m[0] = fminf(m[0], v); }
+    __device__ __forceinline__ float finish() const { return fminf(min3f(m[0], m[1], m[2]), m[3]); }
+};
+
+// --------------------------------------------------- warp and CTA stages
+
+// Butterfly over groups of W consecutive lanes (W a power of two <= 32);
+// every lane of the group ends with the group's result.  All 32 lanes of the
+// warp must call it.
+template <int OP, int W>
+__device__ __forceinline__ float group_tree(float v)
+{
+#pragma unroll
+    for (int off = W / 2; off > 0; off >>= 1)
+        v = Op<OP>::combine(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+
+// Smallest power of two >= v (v in 1..32).
+__host__ __device__ constexpr int pow2ceil(int v) { return v <= 1 ? 1 : 2 * pow2ceil((v + 1) / 2); }
+
+// CTA stage: warp butterfly, lane 0 of each warp to shared memory, barrier,
+// warp 0 folds the NW warp results.  The result is valid in warp 0.  The
+// caller must place a barrier between two uses of the same `s`.
+template <int OP, int NW>
+__device__ __forceinline__ float cta_reduce(float v, float *s)
+{
+    v = group_tree<OP, 32>(v);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0)
+        s[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        v = lane < NW ? s[lane] : Op<OP>::identity();
+        v = group_tree<OP, pow2ceil(NW)>(v);
+    }
+    return v;
+}
+
+// Number of leading elements of p to peel so that the rest is 32-byte
+// aligned (0..7), capped at len.
+__device__ __forceinline__ int64_t head_to_32B(const float *p, int64_t len)
+{
+    const int64_t h = (int64_t)(((32u - ((uint32_t)(uintptr_t)p & 31u)) & 31u) >> 2);
+    return h < len ? h : len;
+}
+
+}  // namespace red

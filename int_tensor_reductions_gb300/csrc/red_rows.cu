@@ -1,0 +1,173 @@
+// red_rows.cu -- per-row sum / max / min of dense row-major and of packed
+// ragged (CSR-offset) fp32 rows, with the optional accum fold.
+//
+// A group of G lanes (G = 1, 2, ..., 32) owns one row at a time; a warp holds
+// 32/G groups working on 32/G consecutive rows, whose bytes are adjacent in
+// memory for both layouts, so a warp's loads stay within one contiguous span.
+// Each lane folds its share of the row with the per-thread fold of Apache TVM
+// docs, "reduction -> sm100_packed", "Algorithm" (chunks of 8 through 256-bit
+// loads into the packed-add or max3/min3 accumulator; the unaligned head and
+// the remainder scalar), with accum folding the old out[r] into the first
+// accumulator slot ("How inputs change the algorithm").  The G lanes then
+// combine through a butterfly of log2(G) levels.  The loop over rows is
+// warp-uniform so that every shuffle has all 32 lanes present.
+//
+// Few long dense rows go to the split-row path instead (several CTAs per row,
+// see red_full.cu).
+#include "red_internal.h"
+#include "red_prims.cuh"
+#include "red.h"
+
+namespace red {
+namespace {
+
+constexpr int ROWS_NT = 256;
+constexpr int ROWS_U = 4;
+
+template <int OP, int G, bool RAGGED>
+__global__ void __launch_bounds__(ROWS_NT)
+rows_kernel(const float *__restrict__ x, const int64_t *__restrict__ off, int64_t rows, int64_t len,
+            int64_t nnz, int accum, float *__restrict__ out)
+{
+    constexpr int GPW = 32 / G;  // rows per warp at a time
+    const int lane = threadIdx.x & 31;
+    const int gl = lane & (G - 1);  // lane within the group
+    const int gw = lane / G;        // group within the warp
+    const int64_t warp = ((int64_t)blockIdx.x * ROWS_NT + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * ROWS_NT) >> 5;
+
+    for (int64_t r0 = warp * GPW; r0 < rows; r0 += nwarps * GPW) {
+        const int64_t r = r0 + gw;
+        const bool live = r < rows;
+        int64_t b = 0, L = 0;
+        if (live) {
+            if (RAGGED) {
+                int64_t ob = off[r], oe = off[r + 1];
+                ob = ob < 0 ? 0 : (ob > nnz ? nnz : ob);
+                oe = oe < 0 ? 0 : (oe > nnz ? nnz : oe);
+                b = ob;
+                L = oe > ob ? oe - ob : 0;
+            } else {
+                b = r * len;
+                L = len;
+            }
+        }
+        const float *p = x + b;
+        Fold<OP> f;
+        f.init();
+        if (live && accum && gl == 0)
+            f.scalar(out[r]);
+        const int64_t h = head_to_32B(p, L);
+        const int64_t nch = (L - h) >> 3;
+        const int64_t t0 = h + (nch << 3);
+        for (int64_t k = gl; k < h; k += G)
+            f.scalar(ld1(p + k));
+        const float *pa = p + h;
+        int64_t c = gl;
+        for (; c + (ROWS_U - 1) * G < nch; c += ROWS_U * G) {
+            float v[ROWS_U][8];
+#pragma unroll
+            for (int u = 0; u < ROWS_U; ++u)
+                ld8(pa + 8 * (c + u * G), v[u]);
+#pragma unroll
+            for (int u = 0; u < ROWS_U; ++u)
+                f.chunk(v[u]);
+        }
+        for (; c < nch; c += G) {
+            float v[8];
+            ld8(pa + 8 * c, v);
+            f.chunk(v);
+        }
+        for (int64_t k = t0 + gl; k < L; k += G)
+            f.scalar(ld1(p + k));
+        const float v = group_tree<OP, G>(f.finish());
+        if (live && gl == 0)
+            out[r] = v;
+    }
+}
+
+template <int OP, int G, bool RAGGED>
+int launch_group(const float *x, const int64_t *off, int64_t rows, int64_t len, int64_t nnz, int accum,
+                 float *out, cudaStream_t s, int sms)
+{
+    static int occ = 0;
+    if (occ == 0)
+        occ = occupancy((const void *)rows_kernel<OP, G, RAGGED>, ROWS_NT);
+    if (occ <= 0)
+        return fail(RED_ECUDA, "row kernel cannot be resident on this device");
+    const int64_t rows_per_cta = (int64_t)(ROWS_NT / 32) * (32 / G);
+    int64_t ctas = (rows + rows_per_cta - 1) / rows_per_cta;
+    const int64_t cap = (int64_t)sms * occ;
+    if (ctas > cap)
+        ctas = cap;
+    if (ctas < 1)
+        ctas = 1;
+    rows_kernel<OP, G, RAGGED><<<(unsigned)ctas, ROWS_NT, 0, s>>>(x, off, rows, len, nnz, accum, out);
+    count_launches(1);
+    return cuda_fail(cudaGetLastError(), "row kernel launch");
+}
+
+template <int OP, bool RAGGED>
+int launch_g(int G, const float *x, const int64_t *off, int64_t rows, int64_t len, int64_t nnz, int accum,
+             float *out, cudaStream_t s, int sms)
+{
+    switch (G) {
+    case 1: return launch_group<OP, 1, RAGGED>(x, off, rows, len, nnz, accum, out, s, sms);
+    case 2: return launch_group<OP, 2, RAGGED>(x, off, rows, len, nnz, accum, out, s, sms);
+    case 4: return launch_group<OP, 4, RAGGED>(x, off, rows, len, nnz, accum, out, s, sms);
+    case 8: return launch_group<OP, 8, RAGGED>(x, off, rows, len, nnz, accum, out, s, sms);
+    case 16: return launch_group<OP, 16, RAGGED>(x, off, rows, len, nnz, accum, out, s, sms);
+    default: return launch_group<OP, 32, RAGGED>(x, off, rows, len, nnz, accum, out, s, sms);
+    }
+}
+
+template <bool RAGGED>
+int launch_op(int op, int G, const float *x, const int64_t *off, int64_t rows, int64_t len, int64_t nnz,
+              int accum, float *out, cudaStream_t s, int sms)
+{
+    switch (op) {
+    case OP_SUM: return launch_g<OP_SUM, RAGGED>(G, x, off, rows, len, nnz, accum, out, s, sms);
+    case OP_MAX: return launch_g<OP_MAX, RAGGED>(G, x, off, rows, len, nnz, accum, out, s, sms);
+    default: return launch_g<OP_MIN, RAGGED>(G, x, off, rows, len, nnz, accum, out, s, sms);
+    }
+}
+
+// Lanes per row for a (mean) row length: about 32 floats per lane, a power of
+// two in 1..32.
+int auto_group(int64_t mean_len)
+{
+    int g = 1;
+    while (g < 32 && (int64_t)g * 64 <= mean_len)
+        g *= 2;
+    return g;
+}
+
+}  // namespace
+
+int launch_rows(int op, const float *x, int64_t rows, int64_t len, int accum, float *out, cudaStream_t s)
+{
+    DeviceInfo di;
+    const int st = device_info(&di);
+    if (st != RED_OK)
+        return st;
+    // Few long rows cannot fill the GPU with one group per row: split each
+    // row over several CTAs.
+    if (knob(RED_KNOB_ROWS_GROUP) == 0 && len >= 8192 && rows < (int64_t)di.sms * 16)
+        return launch_rows_split(op, x, rows, len, accum, out, s, di);
+    const int g = knob(RED_KNOB_ROWS_GROUP) ? knob(RED_KNOB_ROWS_GROUP) : auto_group(len);
+    return launch_op<false>(op, g, x, nullptr, rows, len, 0, accum, out, s, di.sms);
+}
+
+int launch_ragged(int op, const float *x, const int64_t *off, int64_t rows, int64_t nnz, int accum,
+                  float *out, cudaStream_t s)
+{
+    DeviceInfo di;
+    const int st = device_info(&di);
+    if (st != RED_OK)
+        return st;
+    const int g = knob(RED_KNOB_RAGGED_GROUP) ? knob(RED_KNOB_RAGGED_GROUP)
+                                               : auto_group(rows > 0 ? nnz / rows : 0);
+    return launch_op<true>(op, g, x, off, rows, 0, nnz, accum, out, s, di.sms);
+}
+
+}  // namespace red

@@ -1,0 +1,101 @@
+"""The C ABI library loads, exports every function include/red.h declares, and
+rejects bad arguments on the host before touching the GPU (no compute call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "red.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from int_tensor_reductions_gb300 import _build, _binding
+    _build.build_lib()
+    return _binding.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(red_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("red_full", "red_rows", "red_rows_ragged", "red_colprod", "red_set_full_mode",
+              "red_last_error", "red_release_workspace", "red_version"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_version(lib):
+    assert lib.red_version() == 1
+
+
+def _err(lib):
+    return lib.red_last_error().decode()
+
+
+def test_full_rejects_bad_arguments(lib):
+    from int_tensor_reductions_gb300 import RED_EINVAL, RED_SUM, RED_MAX
+    assert lib.red_full(7, 0x1000, 8, 0x2000, None) == RED_EINVAL
+    assert "unknown op" in _err(lib)
+    assert lib.red_full(RED_SUM, 0x1000, -1, 0x2000, None) == RED_EINVAL
+    assert lib.red_full(RED_SUM, None, 8, 0x2000, None) == RED_EINVAL
+    assert lib.red_full(RED_SUM, 0x1000, 8, None, None) == RED_EINVAL
+    assert lib.red_full(RED_SUM, 0x1001, 8, 0x2000, None) == RED_EINVAL  # misaligned x
+    assert lib.red_full(RED_MAX, None, 0, 0x2000, None) == RED_EINVAL    # max of nothing
+    assert "empty" in _err(lib)
+
+
+def test_rows_reject_bad_arguments(lib):
+    from int_tensor_reductions_gb300 import RED_EINVAL, RED_OK, RED_SUM, RED_MIN
+    assert lib.red_rows(RED_SUM, 0x1000, -2, 4, 0, 0x2000, None) == RED_EINVAL
+    assert lib.red_rows(RED_SUM, 0x1000, 2, -4, 0, 0x2000, None) == RED_EINVAL
+    assert lib.red_rows(RED_SUM, 0x1000, 1 << 40, 1 << 40, 0, 0x2000, None) == RED_EINVAL
+    assert lib.red_rows(RED_MIN, 0x1000, 3, 0, 0, 0x2000, None) == RED_EINVAL
+    assert lib.red_rows(RED_SUM, 0x1000, 0, 5, 0, None, None) == RED_OK   # nothing to do
+    assert lib.red_rows(RED_SUM, 0x1000, 3, 0, 1, 0x2000, None) == RED_OK  # accum, empty rows
+    assert lib.red_rows_ragged(RED_SUM, 0x1000, 0x3004, 4, 10, 0, 0x2000, None) == RED_EINVAL
+    assert lib.red_rows_ragged(RED_SUM, 0x1000, None, 4, 10, 0, 0x2000, None) == RED_EINVAL
+    assert lib.red_rows_ragged(9, 0x1000, 0x3000, 4, 10, 0, 0x2000, None) == RED_EINVAL
+
+
+def test_colprod_rejects_and_returns_early(lib):
+    from int_tensor_reductions_gb300 import RED_EINVAL, RED_F32, RED_OK
+    assert lib.red_colprod(5, 0x1000, 4, 4, 0x2000, None) == RED_EINVAL
+    assert lib.red_colprod(RED_F32, 0x1000, -1, 4, 0x2000, None) == RED_EINVAL
+    # pto-isa docs, "TCOLPROD", "Constraints": empty tile -> early return
+    assert lib.red_colprod(RED_F32, None, 0, 4, None, None) == RED_OK
+    assert lib.red_colprod(RED_F32, None, 4, 0, None, None) == RED_OK
+
+
+def test_knobs_and_modes(lib):
+    import int_tensor_reductions_gb300 as itr
+    assert lib.red_set_full_mode(9) == itr.RED_EINVAL
+    for m in (itr.RED_MODE_TWO_PASS, itr.RED_MODE_LAST_BLOCK, itr.RED_MODE_ATOMIC):
+        itr.red_set_full_mode(m)
+        assert itr.red_get_full_mode() == m
+    itr.red_set_full_mode(itr.RED_MODE_AUTO)
+    assert itr.red_get_full_mode() in (1, 2, 3)
+    assert lib.red_set_knob(itr.RED_KNOB_ROWS_GROUP, 3) == itr.RED_EINVAL
+    itr.red_set_knob(itr.RED_KNOB_ROWS_GROUP, 8)
+    assert itr.red_get_knob(itr.RED_KNOB_ROWS_GROUP) == 8
+    itr.red_set_knob(itr.RED_KNOB_ROWS_GROUP, 0)
+    assert lib.red_get_knob(99) == itr.RED_EINVAL
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    import int_tensor_reductions_gb300 as itr
+    with pytest.raises(ValueError):
+        itr.red_full("sum", torch.ones(8))

@@ -1,0 +1,141 @@
+"""red_rows and red_rows_ragged on the GPU against the oracle: tiny and
+ragged shapes (every chunk-of-8 remainder, unaligned row starts), every
+lanes-per-row mapping, the split-row path for few long rows, accum, empty
+rows, and the 65536 x 1024 and 2**22-ragged-row workloads at full size."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import int_tensor_reductions_gb300 as itr
+from int_tensor_reductions_gb300 import synth
+from gpu_util import check_exact, check_sum, lib_ready, to_host
+
+pytestmark = pytest.mark.gpu
+
+OPS = ("sum", "max", "min")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    lib_ready()
+    yield
+    itr.red_set_knob(itr.RED_KNOB_ROWS_GROUP, 0)
+    itr.red_set_knob(itr.RED_KNOB_RAGGED_GROUP, 0)
+
+
+def _dense_case(x2d: torch.Tensor, dst: torch.Tensor, what: str):
+    rows, length = x2d.shape
+    xh, dh = to_host(x2d), to_host(dst)
+    for accum in (False, True):
+        for op in OPS:
+            out = dst.clone()
+            itr.red_rows(op, x2d, accum=accum, out=out)
+            got = to_host(out)
+            if op == "sum":
+                s, a = oracle.rows("sum", xh, rows, length, accum, dh)
+                check_sum(got, s, a, f"{what} sum accum={accum}")
+            else:
+                check_exact(got, oracle.rows(op, xh, rows, length, accum, dh), f"{what} {op} accum={accum}")
+
+
+@pytest.mark.parametrize("rows,length", [
+    (1, 1), (3, 7), (5, 8), (7, 9), (33, 31), (100, 40), (17, 64), (9, 1000), (4, 1024),
+    (3, 5000), (300, 8191), (2, 20000), (1, 100003), (5, 300007),
+])
+def test_dense_shapes(rows, length):
+    x = synth.uniform((rows * length + 1,), -4.0, 4.0, rows + length).cuda()
+    dst = synth.uniform((rows,), -1.0, 1.0, 3).cuda()
+    _dense_case(x[:rows * length].view(rows, length), dst, f"{rows}x{length}")
+    # rows starting at an odd float: every row has a different head peel
+    _dense_case(x[1:].view(rows, length), dst, f"{rows}x{length} shifted")
+
+
+@pytest.mark.parametrize("g", [1, 2, 4, 8, 16, 32])
+def test_dense_every_group_size(g):
+    itr.red_set_knob(itr.RED_KNOB_ROWS_GROUP, g)
+    try:
+        for rows, length in ((257, 13), (130, 77), (64, 1029)):
+            x = synth.normal((rows * length + 3,), g, device="cuda")
+            dst = synth.uniform((rows,), -1.0, 1.0, 4, device="cuda")
+            _dense_case(x[3:].view(rows, length), dst, f"G={g} {rows}x{length}")
+    finally:
+        itr.red_set_knob(itr.RED_KNOB_ROWS_GROUP, 0)
+
+
+def test_dense_len0():
+    x = torch.empty((5, 0), device="cuda")
+    out = torch.full((5,), 2.5, device="cuda")
+    itr.red_rows("sum", x, accum=True, out=out)
+    assert to_host(out).tolist() == [2.5] * 5
+    itr.red_rows("sum", x, out=out)
+    assert to_host(out).tolist() == [0.0] * 5
+    with pytest.raises(itr.RedError):
+        itr.red_rows("max", x, out=out)
+
+
+def test_cfg2_dense_workload():
+    """65536 x 1024 normal(0,1) rows, every op, and sum with accum into a
+    uniform[-1,1) dst, compared row by row in full."""
+    x, dst = synth.cfg2(device="cuda")
+    _dense_case(x, dst, "cfg2")
+
+
+def _ragged_case(x, off, dst, what):
+    xh, oh, dh = to_host(x), to_host(off), to_host(dst)
+    for accum in (False, True):
+        for op in OPS:
+            out = dst.clone()
+            itr.red_rows_ragged(op, x, off, accum=accum, out=out)
+            got = to_host(out)
+            if op == "sum":
+                s, a = oracle.ragged("sum", xh, oh, accum, dh)
+                check_sum(got, s, a, f"{what} sum accum={accum}")
+            else:
+                check_exact(got, oracle.ragged(op, xh, oh, accum, dh), f"{what} {op} accum={accum}")
+
+
+@pytest.mark.parametrize("g", [0, 1, 2, 4, 8, 16, 32])
+def test_ragged_with_empty_rows(g):
+    itr.red_set_knob(itr.RED_KNOB_RAGGED_GROUP, g)
+    try:
+        gen = np.random.default_rng(5 + g)
+        lens = gen.integers(0, 41, size=3001)
+        lens[::13] = 0
+        lens[7] = 300
+        off = np.zeros(lens.size + 1, np.int64)
+        off[1:] = np.cumsum(lens)
+        x = synth.uniform((int(off[-1]),), -4.0, 4.0, 6, device="cuda")
+        dst = synth.uniform((lens.size,), -1.0, 1.0, 8, device="cuda")
+        _ragged_case(x, torch.from_numpy(off).cuda(), dst, f"ragged G={g}")
+    finally:
+        itr.red_set_knob(itr.RED_KNOB_RAGGED_GROUP, 0)
+
+
+def test_ragged_lengths_8_to_40_every_remainder():
+    """One row of every length 8..40 at every start alignment 0..7."""
+    lens = np.array([L for L in range(8, 41) for _ in range(8)], np.int64)
+    off = np.zeros(lens.size + 1, np.int64)
+    off[1:] = np.cumsum(lens)
+    x = synth.uniform((int(off[-1]),), -4.0, 4.0, 10, device="cuda")
+    dst = synth.uniform((lens.size,), -1.0, 1.0, 11, device="cuda")
+    _ragged_case(x, torch.from_numpy(off).cuda(), dst, "lengths 8..40")
+
+
+def test_ragged_all_empty():
+    off = torch.zeros(6, dtype=torch.int64, device="cuda")
+    x = torch.empty(0, device="cuda")
+    out = torch.full((5,), 1.5, device="cuda")
+    itr.red_rows_ragged("max", x, off, out=out)
+    assert to_host(out).tolist() == [-np.inf] * 5
+    itr.red_rows_ragged("min", x, off, out=out)
+    assert to_host(out).tolist() == [np.inf] * 5
+    itr.red_rows_ragged("sum", x, off, out=out)
+    assert to_host(out).tolist() == [0.0] * 5
+
+
+def test_cfg5_ragged_workload():
+    """2**22 rows of lengths 8..40, uniform[-4,4), compared row by row."""
+    x, off = synth.cfg5(device="cuda")
+    dst = synth.uniform((synth.CFG5_ROWS,), -1.0, 1.0, 12, device="cuda")
+    _ragged_case(x, off, dst, "cfg5")

@@ -49,7 +49,13 @@ def test_page_example_16x16():
     x = torch.tensor(cs, dtype=torch.float32, device="cuda").repeat(R, 1).contiguous()
     got = to_host(itr.red_colprod(x))
     ref = np.array([np.float32(e.numerator / e.denominator) for e in exp], np.float32)
-    check_exact(got, ref, "16x16 closed form")
+    # Columns of +-2**k: every partial product is exact in fp32, so the GPU
+    # result must be the closed form bit for bit.  The other columns round
+    # in fp32 along the way: within the 5e-4 relative tolerance of the
+    # exact value.
+    pow2 = [j for j, c in enumerate(cs) if abs(c) in (0.25, 0.5, 1.0, 2.0, 4.0)]
+    check_exact(got[pow2], ref[pow2], "16x16 closed form, power-of-two columns")
+    check_prod(got, [e.numerator / e.denominator for e in exp], "16x16 closed form")
 
 
 def test_early_return_leaves_out_untouched():

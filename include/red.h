@@ -147,6 +147,40 @@ int red_rows_ragged(int op, const float *x, const int64_t *offsets, int64_t rows
  */
 int red_colprod(int dtype, const void *x, int64_t R, int64_t C, void *out, red_stream_t stream);
 
+/*
+ * red_full_noalloc -- red_full for callers that cannot allocate device memory.
+ * The pages have no counterpart of this call; it exists for the library's
+ * users.  red_full allocates a 16 MiB workspace with cudaMalloc on its first
+ * call on a device.  Some callers cannot let a library do that: cudaMalloc
+ * (and cudaFree) may synchronise the whole device, which a latency-bound
+ * serving or real-time loop cannot absorb, and a framework whose own caching
+ * allocator has reserved the device memory, or that enforces a memory budget,
+ * may see the allocation fail or break its accounting.
+ *
+ * This call never allocates: it calls no cudaMalloc, cudaFree or allocating
+ * library routine.  Its scratch is a fixed array in the library's device
+ * memory, RED_NOALLOC_MAX_PARTIALS fp32 partial slots plus one arrival
+ * counter (16 KiB + 256 B), which every GPU that loads the library holds
+ * until the process exits.  The result is the same reduction as red_full
+ * with the last-block grid stage (one kernel; the red_set_full_mode setting
+ * does not apply).
+ *   op, x, n, out, stream   as for red_full (device pointers, async on stream).
+ * Errors: as red_full; in addition RED_EINVAL when the launch would need more
+ * CTAs (partial slots) than the scratch holds -- only possible when
+ * RED_KNOB_FULL_CTAS_PER_SM asks for more than RED_NOALLOC_MAX_PARTIALS CTAs
+ * in all; the message says so.  n itself has no limit beyond red_full's.
+ * Set-up: the first call on a device looks up the scratch array's device
+ * address (cudaGetSymbolAddress, with that device current) and caches it, so
+ * that first call should come before any CUDA stream capture.
+ * Sharing: every call on a device uses the same scratch.  Each call first
+ * clears the counter on its stream (cudaMemsetAsync, which allocates
+ * nothing), and the partials are rewritten before they are read; calls that
+ * overlap on the GPU (different streams, not ordered by events) race and
+ * give wrong results.
+ */
+#define RED_NOALLOC_MAX_PARTIALS 4096
+int red_full_noalloc(int op, const float *x, int64_t n, float *out, red_stream_t stream);
+
 /* Select the grid stage of red_full (enum red_full_mode).  Process-wide.
  * Returns RED_OK, or RED_EINVAL for an unknown mode. */
 int red_set_full_mode(int mode);

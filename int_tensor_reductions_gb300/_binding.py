@@ -20,6 +20,7 @@ _lib = None
 _i64, _int, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
 _SIGNATURES = {
     "red_full": ([_int, _vp, _i64, _vp, _vp], _int),
+    "red_full_noalloc": ([_int, _vp, _i64, _vp, _vp], _int),
     "red_rows": ([_int, _vp, _i64, _i64, _int, _vp, _vp], _int),
     "red_rows_ragged": ([_int, _vp, _vp, _i64, _i64, _int, _vp, _vp], _int),
     "red_colprod": ([_int, _vp, _i64, _i64, _vp, _vp], _int),
@@ -101,6 +102,19 @@ def red_full(op, x: torch.Tensor, out: torch.Tensor | None = None, stream=None) 
     _need(out, "out", (torch.float32,))
     with torch.cuda.device(x.device):
         _check(lib().red_full(_op(op), x.data_ptr(), x.numel(), out.data_ptr(), _stream(stream, x.device)))
+    return out
+
+
+def red_full_noalloc(op, x: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """red_full without any device allocation by the library: its scratch is a
+    fixed array in the library (for callers that cannot let a library call
+    cudaMalloc).  ``out`` must be given, so this wrapper allocates nothing
+    either."""
+    _need(x, "x", (torch.float32,))
+    _need(out, "out", (torch.float32,))
+    with torch.cuda.device(x.device):
+        _check(lib().red_full_noalloc(_op(op), x.data_ptr(), x.numel(), out.data_ptr(),
+                                      _stream(stream, x.device)))
     return out
 
 

@@ -253,6 +253,33 @@ int launch_full(int op, const float *x, int64_t n, float *out, cudaStream_t s)
     return launch_seg_op(op, stage, x, 1, n, (int)ctas, 0, out, ws, s);
 }
 
+int launch_full_scratch(int op, const float *x, int64_t n, float *out, cudaStream_t s, float *part,
+                        unsigned *tick, int64_t max_parts)
+{
+    DeviceInfo di;
+    const int st = device_info(&di);
+    if (st != RED_OK)
+        return st;
+    const int occ = ctas_per_sm(op, STAGE_LAST_BLOCK);
+    if (occ <= 0)
+        return fail(RED_ECUDA, "red_full_noalloc: kernel cannot be resident on this device");
+    const int64_t want = ceil_div(n / 8 + 1, (int64_t)FULL_NT * FULL_U);
+    int64_t ctas = (int64_t)di.sms * occ;
+    if (want < ctas)
+        ctas = want;
+    if (ctas < 1)
+        ctas = 1;
+    if (ctas > max_parts)
+        return fail(RED_EINVAL,
+                    "red_full_noalloc: this launch needs %lld partial slots but the static scratch holds %lld "
+                    "(lower RED_KNOB_FULL_CTAS_PER_SM)",
+                    (long long)ctas, (long long)max_parts);
+    Workspace ws;
+    ws.part = part;
+    ws.tick = tick;
+    return launch_seg_op(op, STAGE_LAST_BLOCK, x, 1, n, (int)ctas, 0, out, ws, s);
+}
+
 int launch_rows_split(int op, const float *x, int64_t rows, int64_t len, int accum, float *out,
                       cudaStream_t s, const DeviceInfo &di)
 {

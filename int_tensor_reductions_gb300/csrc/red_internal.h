@@ -39,6 +39,10 @@ int full_mode();            // resolved grid stage of red_full (1, 2 or 3)
 
 // Launchers: arguments have been validated by the entry points.
 int launch_full(int op, const float *x, int64_t n, float *out, cudaStream_t s);
+// Last-block full reduction with caller-provided scratch (max_parts partial
+// slots and one counter that is zero on entry); allocates nothing.
+int launch_full_scratch(int op, const float *x, int64_t n, float *out, cudaStream_t s, float *part,
+                        unsigned *tick, int64_t max_parts);
 int launch_rows_split(int op, const float *x, int64_t rows, int64_t len, int accum, float *out,
                       cudaStream_t s, const DeviceInfo &di);
 int launch_rows(int op, const float *x, int64_t rows, int64_t len, int accum, float *out,

@@ -60,6 +60,11 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stage-compare", action="store_true")
+    ap.add_argument("--only", default="",
+                    help="comma-separated op families to run (full1, full3, rows2, ragged5, colprod4a, "
+                         "colprod4b); for profiling: the line is then not the benchmark's metric")
+    ap.add_argument("--scale", type=float, default=1.0,
+                    help="fraction of every workload's size (rows / elements); for profiling")
     return ap.parse_args()
 
 
@@ -151,27 +156,43 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside)}
 
 
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The largest x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0])
+
+
+def job_gbs(world: int, step_bytes: int, steps: int, max_ms: float) -> float:
+    """Whole-job GB/s: every rank processed steps x step_bytes in at most max_ms."""
+    return world * step_bytes * steps / (max_ms * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------ the workload
 
 class Workload:
     """Device inputs and outputs of one step and the ops in step order."""
 
-    def __init__(self, device, frac=1.0, host_only=False):
+    def __init__(self, device, frac=1.0, host_only=False, kinds=None):
         import torch
         from int_tensor_reductions_gb300 import synth
         self.torch = torch
         gen_dev = "cpu" if host_only else device
-        f = frac
 
-        def n_of(n):
+        def n_of(n, kind):
+            # workloads left out by `kinds` get token-sized inputs
+            f = frac if (not kinds or kind in kinds) else 1.0 / 65536
             return max(8, int(n * f))
 
-        self.x1 = synth.cfg1(gen_dev, n=n_of(synth.CFG1_N))
-        self.x2, self.dst2 = synth.cfg2(gen_dev, rows=n_of(synth.CFG2_ROWS), length=synth.CFG2_LEN)
-        self.x3 = synth.cfg3(gen_dev, n=n_of(synth.CFG3_N))
-        self.x4a = synth.cfg4a(gen_dev, R=n_of(synth.CFG4A_R), C=synth.CFG4A_C)
-        self.x4b = synth.cfg4b(gen_dev, R=max(1, int(synth.CFG4B_R * f)), C=synth.CFG4B_C)
-        self.x5, self.off5 = synth.cfg5(gen_dev, rows=n_of(synth.CFG5_ROWS))
+        self.x1 = synth.cfg1(gen_dev, n=n_of(synth.CFG1_N, "full1"))
+        self.x2, self.dst2 = synth.cfg2(gen_dev, rows=n_of(synth.CFG2_ROWS, "rows2"), length=synth.CFG2_LEN)
+        self.x3 = synth.cfg3(gen_dev, n=n_of(synth.CFG3_N, "full3"))
+        self.x4a = synth.cfg4a(gen_dev, R=n_of(synth.CFG4A_R, "colprod4a"), C=synth.CFG4A_C)
+        self.x4b = synth.cfg4b(gen_dev, R=n_of(synth.CFG4B_R, "colprod4b"), C=synth.CFG4B_C)
+        self.x5, self.off5 = synth.cfg5(gen_dev, rows=n_of(synth.CFG5_ROWS, "ragged5"))
         self.inputs = [self.x1, self.x2, self.dst2, self.x3, self.x4a, self.x4b, self.x5, self.off5]
         r2, l2 = self.x2.shape
         n5 = self.off5.numel() - 1
@@ -315,7 +336,15 @@ def run_ours(args):
     _build.build_lib()
     stream = torch.cuda.current_stream(dev)
 
-    w = Workload(dev)
+    only = [k for k in args.only.split(",") if k]
+    w = Workload(dev, frac=args.scale, kinds=only or None)
+    partial = bool(only) or args.scale != 1.0
+    if only:
+        w.plan = [(name, key) for name, key in w.plan if name.split(" ")[0] in only]
+        w.step_bytes = sum(w.bytes_of[k] for _, k in w.plan)
+    if partial:
+        args.no_e2e = args.no_cpu_baseline = True
+        args.no_stage_compare = args.no_stage_compare or "full3" not in (only or ["full3"])
     calls = [(name, key, w.gpu_call(name)) for name, key in w.plan]
     torch.cuda.synchronize()
 
@@ -357,24 +386,20 @@ def run_ours(args):
     launches = itr.red_launch_count() - launches0
     sampler.mark(h0, h1)
     clocks = sampler.stop()
-    total_ms = t_begin.elapsed_time(t_end)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t[0])
+    total_ms = max_over_ranks(t_begin.elapsed_time(t_end), dist, dev)
     per_op = {}
     for i, (name, key, _) in enumerate(calls):
         ms = [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(K)]
         mean = sum(ms) / K
         per_op[name] = {"ms": round(mean, 5), "gbs": round(w.bytes_of[key] / (mean * 1e-3) / 1e9, 1)}
 
-    value = world * w.step_bytes * K / (total_ms * 1e-3) / 1e9
+    value = job_gbs(world, w.step_bytes, K, total_ms)
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"] if peaks and "hbm_gbs" in peaks else FALLBACK_HBM_GBS
     peak_src = "measured" if peaks and "hbm_gbs" in peaks else "fallback"
-    dom = [per_op[n]["ms"] for n in ("full3 sum", "full3 max", "full3 min")]
-    dom_ms = sum(dom) / len(dom)
-    achieved = w.bytes_of["full3"] / (dom_ms * 1e-3) / 1e9
+    dom = [per_op[n]["ms"] for n in ("full3 sum", "full3 max", "full3 min") if n in per_op]
+    dom_ms = sum(dom) / len(dom) if dom else float("nan")
+    achieved = w.bytes_of["full3"] / (dom_ms * 1e-3) / 1e9 if dom else None
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -390,13 +415,14 @@ def run_ours(args):
         },
         "frac_of_nominal_8TBs": round(value / world / NOMINAL_HBM_GBS, 4),
         "roofline": {
-            "bound": "hbm", "kernel": DOMINANT, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "peak_source": peak_src,
-            "frac_of_nominal_8TBs": round(achieved / NOMINAL_HBM_GBS, 4),
+            "bound": "hbm", "kernel": DOMINANT, "achieved": achieved and round(achieved, 1), "peak": peak,
+            "unit": "GB/s", "frac": achieved and round(achieved / peak, 4), "peak_source": peak_src,
+            "frac_of_nominal_8TBs": achieved and round(achieved / NOMINAL_HBM_GBS, 4),
             "traffic": traffic_per_launch(), "algorithmic_bytes_per_launch": w.bytes_of["full3"],
         },
         "ops": per_op,
         "gpu_launches": int(launches),
+        "partial": {"only": only, "scale": args.scale} if partial else None,
         "clocks": clocks,
     }
 
@@ -472,12 +498,8 @@ def run_e2e(w, calls, stream, steps, world, dist, dev):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t[0])
-    value = world * w.step_bytes * steps / (ms * 1e-3) / 1e9
+    ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    value = job_gbs(world, w.step_bytes, steps, ms)
     return {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "ms_per_step": round(ms / steps, 3)}
 

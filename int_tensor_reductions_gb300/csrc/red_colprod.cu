@@ -162,15 +162,25 @@ int launch_cp(const T *x, int64_t R, int64_t C, T *out, cudaStream_t s, const De
     const int64_t tiles = (C + tile_cols - 1) / tile_cols;
     if (tiles > 0x7fffffffLL)
         return fail(RED_EINVAL, "red_colprod: C too large");
-    // Row splits: enough CTAs to fill the machine, each warp keeping at least
-    // CP_U rows, the partials within the workspace, one counter per tile.
+    // Row splits: each warp keeps at least CP_U rows, and among those counts
+    // the one whose CTAs fill whole waves best.  With `slots` resident CTAs,
+    // s splits take ceil(tiles*s/slots) waves of R/s rows each, so minimise
+    // ceil(tiles*s/slots)/s (the smallest s on ties: fewer partials).
     int64_t splits = knob(RED_KNOB_COLPROD_SPLITS);
     if (splits <= 0) {
-        const int64_t target = (int64_t)di.sms * occ;
-        splits = (target + tiles - 1) / tiles;
-        const int64_t max_by_rows = R / (CP_WY * CP_U);
-        if (splits > max_by_rows)
-            splits = max_by_rows;
+        const int64_t slots = (int64_t)di.sms * occ;
+        int64_t smax = R / (CP_WY * CP_U);
+        if (smax > 4096)
+            smax = 4096;
+        splits = 1;
+        double best = (double)((tiles + slots - 1) / slots);
+        for (int64_t sp = 2; sp <= smax; ++sp) {
+            const double t = (double)((tiles * sp + slots - 1) / slots) / (double)sp;
+            if (t < best * 0.999) {
+                best = t;
+                splits = sp;
+            }
+        }
     }
     if (splits > R)
         splits = R;

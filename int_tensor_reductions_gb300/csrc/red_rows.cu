@@ -5,10 +5,15 @@
 // 32/G groups working on 32/G consecutive rows, whose bytes are adjacent in
 // memory for both layouts, so a warp's loads stay within one contiguous span.
 // Each lane folds its share of the row with the per-thread fold of Apache TVM
-// docs, "reduction -> sm100_packed", "Algorithm" (chunks of 8 through 256-bit
-// loads into the packed-add or max3/min3 accumulator; the unaligned head and
-// the remainder scalar), with accum folding the old out[r] into the first
-// accumulator slot ("How inputs change the algorithm").  The G lanes then
+// docs, "reduction -> sm100_packed", "Algorithm" (chunks of 8 into the
+// packed-add or max3/min3 accumulator), with accum folding the old out[r]
+// into the first accumulator slot ("How inputs change the algorithm").  The
+// chunks are the aligned 8-float blocks that hold the row, each read with one
+// 256-bit load; the row's unaligned head and tail are the masked parts of its
+// first and last block (other rows' elements there count as the identity),
+// so no row needs a scalar loop and a short row's loads all go out at once.
+// A block that reaches past either end of x is read element by element, so
+// every load stays inside x.  The G lanes then
 // combine through a butterfly of log2(G) levels.  The loop over rows is
 // warp-uniform so that every shuffle has all 32 lanes present.
 //
@@ -25,61 +30,89 @@ constexpr int ROWS_NT = 256;
 constexpr int ROWS_U = 4;
 
 template <int OP, int G, bool RAGGED>
-__global__ void __launch_bounds__(ROWS_NT)
+__global__ void __launch_bounds__(ROWS_NT, 3)
 rows_kernel(const float *__restrict__ x, const int64_t *__restrict__ off, int64_t rows, int64_t len,
             int64_t nnz, int accum, float *__restrict__ out)
 {
-    constexpr int GPW = 32 / G;  // rows per warp at a time
+    constexpr int GPW = 32 / G;           // rows per warp at a time
+    constexpr int U = G == 1 ? 6 : ROWS_U; // blocks in flight per lane (a 40-float row spans <= 6)
+    const int64_t total = RAGGED ? nnz : rows * len;
+    const int64_t x_mis = (int64_t)(((uintptr_t)x & 31u) >> 2);  // x's offset from a 32-byte boundary
+    const float ident = Op<OP>::identity();
     const int lane = threadIdx.x & 31;
     const int gl = lane & (G - 1);  // lane within the group
     const int gw = lane / G;        // group within the warp
     const int64_t warp = ((int64_t)blockIdx.x * ROWS_NT + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * ROWS_NT) >> 5;
 
-    for (int64_t r0 = warp * GPW; r0 < rows; r0 += nwarps * GPW) {
+    // Row r's extent; for ragged rows the offsets of the next row this lane
+    // will fold are loaded one iteration ahead, so that the row loads never
+    // wait behind a dependent offsets load.
+    auto extent = [&](int64_t r, int64_t &b, int64_t &L) {
+        b = 0;
+        L = 0;
+        if (r >= rows)
+            return;
+        if (RAGGED) {
+            int64_t ob = off[r], oe = off[r + 1];
+            ob = ob < 0 ? 0 : (ob > nnz ? nnz : ob);
+            oe = oe < 0 ? 0 : (oe > nnz ? nnz : oe);
+            b = ob;
+            L = oe > ob ? oe - ob : 0;
+        } else {
+            b = r * len;
+            L = len;
+        }
+    };
+    const int64_t stride = nwarps * GPW;
+    int64_t b_next, L_next;
+    extent(warp * GPW + gw, b_next, L_next);
+    for (int64_t r0 = warp * GPW; r0 < rows; r0 += stride) {
         const int64_t r = r0 + gw;
         const bool live = r < rows;
-        int64_t b = 0, L = 0;
-        if (live) {
-            if (RAGGED) {
-                int64_t ob = off[r], oe = off[r + 1];
-                ob = ob < 0 ? 0 : (ob > nnz ? nnz : ob);
-                oe = oe < 0 ? 0 : (oe > nnz ? nnz : oe);
-                b = ob;
-                L = oe > ob ? oe - ob : 0;
-            } else {
-                b = r * len;
-                L = len;
-            }
-        }
-        const float *p = x + b;
+        const int64_t b = b_next, L = L_next;
+        extent(r + stride, b_next, L_next);
         Fold<OP> f;
         f.init();
         if (live && accum && gl == 0)
             f.scalar(out[r]);
-        const int64_t h = head_to_32B(p, L);
-        const int64_t nch = (L - h) >> 3;
-        const int64_t t0 = h + (nch << 3);
-        for (int64_t k = gl; k < h; k += G)
-            f.scalar(ld1(p + k));
-        const float *pa = p + h;
-        int64_t c = gl;
-        for (; c + (ROWS_U - 1) * G < nch; c += ROWS_U * G) {
-            float v[ROWS_U][8];
+        if (L > 0) {
+            // Row [b, e) as the aligned 8-float blocks that hold it: block c
+            // covers [bs + 8c, bs + 8c + 8).  Lane gl takes blocks gl, gl+G,
+            // ..., U of them in flight; only the first and last block hold
+            // elements of other rows, which are replaced by the identity.
+            const int64_t e = b + L;
+            const int64_t bs = ((b + x_mis) & ~int64_t(7)) - x_mis;
+            const int64_t nblk = (e - bs + 7) >> 3;
+            if (bs >= 0 && bs + 8 * nblk <= total) {
+                const int head = (int)(b - bs);                    // masked slots of block 0
+                const int tail = (int)(e - (bs + 8 * (nblk - 1))); // live slots of the last block
+                const float *q = x + bs;
+                for (int64_t c0 = gl; c0 < nblk; c0 += (int64_t)U * G) {
+                    float v[U][8];
 #pragma unroll
-            for (int u = 0; u < ROWS_U; ++u)
-                ld8(pa + 8 * (c + u * G), v[u]);
+                    for (int u = 0; u < U; ++u)
+                        if (c0 + u * G < nblk)
+                            ld8(q + 8 * (c0 + u * G), v[u]);
 #pragma unroll
-            for (int u = 0; u < ROWS_U; ++u)
-                f.chunk(v[u]);
+                    for (int u = 0; u < U; ++u) {
+                        const int64_t c = c0 + u * G;
+                        if (c < nblk) {
+                            const int lo = c == 0 ? head : 0;
+                            const int hi = c == nblk - 1 ? tail : 8;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                v[u][j] = (j >= lo && j < hi) ? v[u][j] : ident;
+                            f.chunk(v[u]);
+                        }
+                    }
+                }
+            } else {
+                // a row in x's first or last partial 32-byte block
+                for (int64_t k = b + gl; k < e; k += G)
+                    f.scalar(ld1(x + k));
+            }
         }
-        for (; c < nch; c += G) {
-            float v[8];
-            ld8(pa + 8 * c, v);
-            f.chunk(v);
-        }
-        for (int64_t k = t0 + gl; k < L; k += G)
-            f.scalar(ld1(p + k));
         const float v = group_tree<OP, G>(f.finish());
         if (live && gl == 0)
             out[r] = v;

@@ -112,6 +112,35 @@ def test_ragged_with_empty_rows(g):
         itr.red_set_knob(itr.RED_KNOB_RAGGED_GROUP, 0)
 
 
+@pytest.mark.parametrize("g", [0, 1, 32])
+def test_ragged_long_row_among_short_ones(g):
+    """Short and empty rows around one 20000-float row and a 77-float row,
+    on a base that is not 32-byte aligned."""
+    itr.red_set_knob(itr.RED_KNOB_RAGGED_GROUP, g)
+    try:
+        gen = np.random.default_rng(40 + g)
+        lens = gen.integers(0, 41, size=2000)
+        lens[::11] = 0
+        lens[300] = 20000
+        lens[1999] = 77
+        off = np.zeros(lens.size + 1, np.int64)
+        off[1:] = np.cumsum(lens)
+        x = synth.uniform((int(off[-1]) + 1,), -4.0, 4.0, 41, device="cuda")[1:]
+        dst = synth.uniform((lens.size,), -1.0, 1.0, 42, device="cuda")
+        _ragged_case(x, torch.from_numpy(off).cuda(), dst, f"G={g} long row")
+    finally:
+        itr.red_set_knob(itr.RED_KNOB_RAGGED_GROUP, 0)
+
+
+def test_dense_short_rows_many():
+    """2**17 dense rows of 1, 7 and 24 floats (one lane per row)."""
+    for length in (1, 7, 24):
+        rows = 1 << 17
+        x = synth.uniform((rows * length + 1,), -4.0, 4.0, length, device="cuda")[1:]
+        dst = synth.uniform((rows,), -1.0, 1.0, 43, device="cuda")
+        _dense_case(x.view(rows, length), dst, f"{rows}x{length}")
+
+
 def test_ragged_lengths_8_to_40_every_remainder():
     """One row of every length 8..40 at every start alignment 0..7."""
     lens = np.array([L for L in range(8, 41) for _ in range(8)], np.int64)

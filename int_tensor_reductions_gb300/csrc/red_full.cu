@@ -22,7 +22,7 @@
 namespace red {
 namespace {
 
-constexpr int FULL_NT = 256;   // threads per CTA
+constexpr int FULL_NT = 512;   // threads per CTA (2 resident per SM: 1024 threads)
 constexpr int FULL_U = 4;      // 256-bit loads in flight per thread
 
 enum : int { STAGE_TWO_PASS = 1, STAGE_LAST_BLOCK = 2, STAGE_ATOMIC = 3 };

@@ -30,12 +30,13 @@ constexpr int ROWS_NT = 256;
 constexpr int ROWS_U = 4;
 
 template <int OP, int G, bool RAGGED>
-__global__ void __launch_bounds__(ROWS_NT, 3)
+__global__ void __launch_bounds__(ROWS_NT, G == 1 ? 3 : 4)
 rows_kernel(const float *__restrict__ x, const int64_t *__restrict__ off, int64_t rows, int64_t len,
             int64_t nnz, int accum, float *__restrict__ out)
 {
     constexpr int GPW = 32 / G;           // rows per warp at a time
-    constexpr int U = G == 1 ? 6 : ROWS_U; // blocks in flight per lane (a 40-float row spans <= 6)
+    constexpr int U = ROWS_U;              // blocks in flight per lane
+    constexpr int SHORT_BLKS = 6;          // a row of <= 41 floats spans <= 6 blocks
     const int64_t total = RAGGED ? nnz : rows * len;
     const int64_t x_mis = (int64_t)(((uintptr_t)x & 31u) >> 2);  // x's offset from a 32-byte boundary
     const float ident = Op<OP>::identity();
@@ -84,7 +85,42 @@ rows_kernel(const float *__restrict__ x, const int64_t *__restrict__ off, int64_
             const int64_t e = b + L;
             const int64_t bs = ((b + x_mis) & ~int64_t(7)) - x_mis;
             const int64_t nblk = (e - bs + 7) >> 3;
-            if (bs >= 0 && bs + 8 * nblk <= total) {
+            if constexpr (G == 1) {
+                if (bs >= 0 && bs + 8 * nblk <= total) {
+                    // One lane per row: the row in pieces of SHORT_BLKS blocks
+                    // (a row of <= 41 floats is one piece), every load of a
+                    // piece in flight at once, 32-bit index math within it.
+                    // Block u of a piece keeps slots [lo, erel - 8u) with
+                    // lo = head for the row's first block, else 0.
+                    const int head = (int)(b - bs);
+                    for (int64_t p0 = 0; p0 < nblk; p0 += SHORT_BLKS) {
+                        const int64_t left = e - (bs + 8 * p0);
+                        const int erel = left < 8 * SHORT_BLKS ? (int)left : 8 * SHORT_BLKS;
+                        const int lo0 = p0 == 0 ? head : 0;
+                        const float *q = x + bs + 8 * p0;
+                        float v[SHORT_BLKS][8];
+#pragma unroll
+                        for (int u = 0; u < SHORT_BLKS; ++u)
+                            if (8 * u < erel)
+                                ld8(q + 8 * u, v[u]);
+#pragma unroll
+                        for (int u = 0; u < SHORT_BLKS; ++u) {
+                            if (8 * u < erel) {
+                                const int hi = erel - 8 * u;
+                                const int lo = u == 0 ? lo0 : 0;
+#pragma unroll
+                                for (int j = 0; j < 8; ++j)
+                                    v[u][j] = (j >= lo && j < hi) ? v[u][j] : ident;
+                                f.chunk(v[u]);
+                            }
+                        }
+                    }
+                } else {
+                    // a row in x's first or last partial 32-byte block
+                    for (int64_t k = b; k < e; ++k)
+                        f.scalar(ld1(x + k));
+                }
+            } else if (bs >= 0 && bs + 8 * nblk <= total) {
                 const int head = (int)(b - bs);                    // masked slots of block 0
                 const int tail = (int)(e - (bs + 8 * (nblk - 1))); // live slots of the last block
                 const float *q = x + bs;

@@ -14,8 +14,8 @@
 //   block reduce in the Triton vector-accumulation blog post (imxueqiu.com),
 //   C version: warp tree, lane 0 of each warp to shared memory, barrier,
 //   second warp tree.
-// * Streaming vector loads: 256-bit (8 x fp32) and 128-bit, read-only path,
-//   no L1 allocation (every byte is read once).
+// * Streaming vector loads: 256-bit (8 x fp32), 128-bit and 64-bit,
+//   read-only path, no L1 allocation (every byte is read once).
 #pragma once
 
 #include <cstdint>
@@ -89,6 +89,23 @@ __device__ __forceinline__ void ld4u(const uint32_t *p, uint32_t (&v)[4])
                  : "l"(p));
 }
 
+// 4 (16-byte aligned) and 2 (8-byte aligned) consecutive floats.
+__device__ __forceinline__ float4 ld4f(const float *p)
+{
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float2 ld2f(const float *p)
+{
+    float2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ float ld1(const float *p) { return __ldg(p); }
 
 // ------------------------------------------------------ operator traits
@@ -138,6 +155,13 @@ struct Fold<OP_SUM> {
             a[k] = add_f32x2(a[k], make_float2(v[2 * k], v[2 * k + 1]));
     }
     __device__ __forceinline__ void scalar(float v) { a[0].x = add_ftz(a[0].x, v); }
+    // pieces of a row's unaligned head or tail: 2 or 4 values
+    __device__ __forceinline__ void pair(float2 v) { a[1] = add_f32x2(a[1], v); }
+    __device__ __forceinline__ void quad(float4 v)
+    {
+        a[2] = add_f32x2(a[2], make_float2(v.x, v.y));
+        a[3] = add_f32x2(a[3], make_float2(v.z, v.w));
+    }
     __device__ __forceinline__ float finish() const
     {
         float2 s01 = add_f32x2(a[0], a[1]);  // (0,1) + (2,3)
@@ -164,6 +188,12 @@ struct Fold<OP_MAX> {
             m[k] = max3f(m[k], v[2 * k], v[2 * k + 1]);
     }
     __device__ __forceinline__ void scalar(float v) { m[0] = fmaxf(m[0], v); }
+    __device__ __forceinline__ void pair(float2 v) { m[1] = max3f(m[1], v.x, v.y); }
+    __device__ __forceinline__ void quad(float4 v)
+    {
+        m[2] = max3f(m[2], v.x, v.y);
+        m[3] = max3f(m[3], v.z, v.w);
+    }
     __device__ __forceinline__ float finish() const { return fmaxf(max3f(m[0], m[1], m[2]), m[3]); }
 };
 
@@ -183,6 +213,12 @@ struct Fold<OP_MIN> {
             m[k] = min3f(m[k], v[2 * k], v[2 * k + 1]);
     }
     __device__ __forceinline__ void scalar(float v) { m[0] = fminf(m[0], v); }
+    __device__ __forceinline__ void pair(float2 v) { m[1] = min3f(m[1], v.x, v.y); }
+    __device__ __forceinline__ void quad(float4 v)
+    {
+        m[2] = min3f(m[2], v.x, v.y);
+        m[3] = min3f(m[3], v.z, v.w);
+    }
     __device__ __forceinline__ float finish() const { return fminf(min3f(m[0], m[1], m[2]), m[3]); }
 };
 

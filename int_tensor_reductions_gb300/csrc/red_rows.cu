@@ -36,7 +36,6 @@ rows_kernel(const float *__restrict__ x, const int64_t *__restrict__ off, int64_
 {
     constexpr int GPW = 32 / G;           // rows per warp at a time
     constexpr int U = ROWS_U;              // blocks in flight per lane
-    constexpr int SHORT_BLKS = 6;          // a row of <= 41 floats spans <= 6 blocks
     const int64_t total = RAGGED ? nnz : rows * len;
     const int64_t x_mis = (int64_t)(((uintptr_t)x & 31u) >> 2);  // x's offset from a 32-byte boundary
     const float ident = Op<OP>::identity();
@@ -86,37 +85,52 @@ rows_kernel(const float *__restrict__ x, const int64_t *__restrict__ off, int64_
             const int64_t bs = ((b + x_mis) & ~int64_t(7)) - x_mis;
             const int64_t nblk = (e - bs + 7) >> 3;
             if constexpr (G == 1) {
-                if (bs >= 0 && bs + 8 * nblk <= total) {
-                    // One lane per row: the row in pieces of SHORT_BLKS blocks
-                    // (a row of <= 41 floats is one piece), every load of a
-                    // piece in flight at once, 32-bit index math within it.
-                    // Block u of a piece keeps slots [lo, erel - 8u) with
-                    // lo = head for the row's first block, else 0.
-                    const int head = (int)(b - bs);
-                    for (int64_t p0 = 0; p0 < nblk; p0 += SHORT_BLKS) {
-                        const int64_t left = e - (bs + 8 * p0);
-                        const int erel = left < 8 * SHORT_BLKS ? (int)left : 8 * SHORT_BLKS;
-                        const int lo0 = p0 == 0 ? head : 0;
-                        const float *q = x + bs + 8 * p0;
-                        float v[SHORT_BLKS][8];
+                // One lane per row, every load inside the row: the aligned
+                // interior [a, z) as 256-bit blocks, the unaligned head
+                // [b, a) and tail [z, e) (0..7 floats each) as at most one
+                // 1-, 2- and 4-float piece each, chosen by the bits of their
+                // lengths so that each piece is naturally aligned.
+                const int64_t a = ((b + x_mis + 7) & ~int64_t(7)) - x_mis;
+                const int64_t z = ((e + x_mis) & ~int64_t(7)) - x_mis;
+                if (a <= z) {
+                    const int h = (int)(a - b), t = (int)(e - z);
+                    const float *ph = x + b, *pt = x + z;
+                    float hs = ident, ts = ident;
+                    float2 h2 = make_float2(ident, ident), t2 = h2;
+                    float4 h4 = make_float4(ident, ident, ident, ident), t4 = h4;
+                    if (h & 1)
+                        hs = ld1(ph);
+                    if (h & 2)
+                        h2 = ld2f(ph + (h & 1));
+                    if (h & 4)
+                        h4 = ld4f(ph + (h & 3));
+                    if (t & 4)
+                        t4 = ld4f(pt);
+                    if (t & 2)
+                        t2 = ld2f(pt + (t & 4));
+                    if (t & 1)
+                        ts = ld1(pt + (t & 6));
+                    const int64_t nfull = (z - a) >> 3;
+                    const float *q = x + a;
+                    for (int64_t c0 = 0; c0 < nfull; c0 += U) {
+                        float v[U][8];
 #pragma unroll
-                        for (int u = 0; u < SHORT_BLKS; ++u)
-                            if (8 * u < erel)
-                                ld8(q + 8 * u, v[u]);
+                        for (int u = 0; u < U; ++u)
+                            if (c0 + u < nfull)
+                                ld8(q + 8 * (c0 + u), v[u]);
 #pragma unroll
-                        for (int u = 0; u < SHORT_BLKS; ++u) {
-                            if (8 * u < erel) {
-                                const int hi = erel - 8 * u;
-                                const int lo = u == 0 ? lo0 : 0;
-#pragma unroll
-                                for (int j = 0; j < 8; ++j)
-                                    v[u][j] = (j >= lo && j < hi) ? v[u][j] : ident;
+                        for (int u = 0; u < U; ++u)
+                            if (c0 + u < nfull)
                                 f.chunk(v[u]);
-                            }
-                        }
                     }
+                    f.scalar(hs);
+                    f.scalar(ts);
+                    f.pair(h2);
+                    f.pair(t2);
+                    f.quad(h4);
+                    f.quad(t4);
                 } else {
-                    // a row in x's first or last partial 32-byte block
+                    // the whole row inside one 32-byte block (fewer than 8 floats)
                     for (int64_t k = b; k < e; ++k)
                         f.scalar(ld1(x + k));
                 }

@@ -8,14 +8,14 @@
 // docs, "reduction -> sm100_packed", "Algorithm" (chunks of 8 into the
 // packed-add or max3/min3 accumulator), with accum folding the old out[r]
 // into the first accumulator slot ("How inputs change the algorithm").  The
-// chunks are the aligned 8-float blocks that hold the row, each read with one
-// 256-bit load; the row's unaligned head and tail are the masked parts of its
-// first and last block (other rows' elements there count as the identity),
-// so no row needs a scalar loop and a short row's loads all go out at once.
-// A block that reaches past either end of x is read element by element, so
-// every load stays inside x.  The G lanes then
-// combine through a butterfly of log2(G) levels.  The loop over rows is
-// warp-uniform so that every shuffle has all 32 lanes present.
+// chunks are the row's 32-byte aligned interior blocks, one 256-bit load
+// each; the page's "remainder" is the row's unaligned head and tail, read as
+// at most three naturally aligned 1-, 2- and 4-float pieces each, so no row
+// needs a scalar loop, a short row's loads all go out at once, and every load
+// lies inside the row.  The G lanes then combine through a butterfly of
+// log2(G) levels.  The loop over rows is warp-uniform so that every shuffle
+// has all 32 lanes present; ragged offsets are clamped into [0, nnz] and the
+// next row's offsets are fetched one iteration ahead.
 //
 // Few long dense rows go to the split-row path instead (several CTAs per row,
 // see red_full.cu).
@@ -30,13 +30,12 @@ constexpr int ROWS_NT = 256;
 constexpr int ROWS_U = 4;
 
 template <int OP, int G, bool RAGGED>
-__global__ void __launch_bounds__(ROWS_NT, G == 1 ? 3 : 4)
+__global__ void __launch_bounds__(ROWS_NT, 3)
 rows_kernel(const float *__restrict__ x, const int64_t *__restrict__ off, int64_t rows, int64_t len,
             int64_t nnz, int accum, float *__restrict__ out)
 {
     constexpr int GPW = 32 / G;           // rows per warp at a time
     constexpr int U = ROWS_U;              // blocks in flight per lane
-    const int64_t total = RAGGED ? nnz : rows * len;
     const int64_t x_mis = (int64_t)(((uintptr_t)x & 31u) >> 2);  // x's offset from a 32-byte boundary
     const float ident = Op<OP>::identity();
     const int lane = threadIdx.x & 31;
@@ -77,88 +76,60 @@ rows_kernel(const float *__restrict__ x, const int64_t *__restrict__ off, int64_
         if (live && accum && gl == 0)
             f.scalar(out[r]);
         if (L > 0) {
-            // Row [b, e) as the aligned 8-float blocks that hold it: block c
-            // covers [bs + 8c, bs + 8c + 8).  Lane gl takes blocks gl, gl+G,
-            // ..., U of them in flight; only the first and last block hold
-            // elements of other rows, which are replaced by the identity.
+            // Row [b, e): the aligned interior [a, z) as 256-bit blocks spread
+            // over the group's lanes (U in flight per lane), the unaligned
+            // head [b, a) and tail [z, e) (0..7 floats each) as at most one
+            // 1-, 2- and 4-float piece each, chosen by the bits of their
+            // lengths so that every piece is naturally aligned.  Every load
+            // lies inside the row.
             const int64_t e = b + L;
-            const int64_t bs = ((b + x_mis) & ~int64_t(7)) - x_mis;
-            const int64_t nblk = (e - bs + 7) >> 3;
-            if constexpr (G == 1) {
-                // One lane per row, every load inside the row: the aligned
-                // interior [a, z) as 256-bit blocks, the unaligned head
-                // [b, a) and tail [z, e) (0..7 floats each) as at most one
-                // 1-, 2- and 4-float piece each, chosen by the bits of their
-                // lengths so that each piece is naturally aligned.
-                const int64_t a = ((b + x_mis + 7) & ~int64_t(7)) - x_mis;
-                const int64_t z = ((e + x_mis) & ~int64_t(7)) - x_mis;
-                if (a <= z) {
-                    const int h = (int)(a - b), t = (int)(e - z);
-                    const float *ph = x + b, *pt = x + z;
-                    float hs = ident, ts = ident;
-                    float2 h2 = make_float2(ident, ident), t2 = h2;
-                    float4 h4 = make_float4(ident, ident, ident, ident), t4 = h4;
+            const int64_t a = ((b + x_mis + 7) & ~int64_t(7)) - x_mis;
+            const int64_t z = ((e + x_mis) & ~int64_t(7)) - x_mis;
+            if (a <= z) {
+                float hs = ident, ts = ident;
+                float2 h2 = make_float2(ident, ident), t2 = h2;
+                float4 h4 = make_float4(ident, ident, ident, ident), t4 = h4;
+                if (gl == 0) {
+                    const int h = (int)(a - b);
+                    const float *ph = x + b;
                     if (h & 1)
                         hs = ld1(ph);
                     if (h & 2)
                         h2 = ld2f(ph + (h & 1));
                     if (h & 4)
                         h4 = ld4f(ph + (h & 3));
+                }
+                if (gl == G - 1) {
+                    const int t = (int)(e - z);
+                    const float *pt = x + z;
                     if (t & 4)
                         t4 = ld4f(pt);
                     if (t & 2)
                         t2 = ld2f(pt + (t & 4));
                     if (t & 1)
                         ts = ld1(pt + (t & 6));
-                    const int64_t nfull = (z - a) >> 3;
-                    const float *q = x + a;
-                    for (int64_t c0 = 0; c0 < nfull; c0 += U) {
-                        float v[U][8];
-#pragma unroll
-                        for (int u = 0; u < U; ++u)
-                            if (c0 + u < nfull)
-                                ld8(q + 8 * (c0 + u), v[u]);
-#pragma unroll
-                        for (int u = 0; u < U; ++u)
-                            if (c0 + u < nfull)
-                                f.chunk(v[u]);
-                    }
-                    f.scalar(hs);
-                    f.scalar(ts);
-                    f.pair(h2);
-                    f.pair(t2);
-                    f.quad(h4);
-                    f.quad(t4);
-                } else {
-                    // the whole row inside one 32-byte block (fewer than 8 floats)
-                    for (int64_t k = b; k < e; ++k)
-                        f.scalar(ld1(x + k));
                 }
-            } else if (bs >= 0 && bs + 8 * nblk <= total) {
-                const int head = (int)(b - bs);                    // masked slots of block 0
-                const int tail = (int)(e - (bs + 8 * (nblk - 1))); // live slots of the last block
-                const float *q = x + bs;
-                for (int64_t c0 = gl; c0 < nblk; c0 += (int64_t)U * G) {
+                const int64_t nfull = (z - a) >> 3;
+                const float *q = x + a;
+                for (int64_t c0 = gl; c0 < nfull; c0 += (int64_t)U * G) {
                     float v[U][8];
 #pragma unroll
                     for (int u = 0; u < U; ++u)
-                        if (c0 + u * G < nblk)
+                        if (c0 + u * G < nfull)
                             ld8(q + 8 * (c0 + u * G), v[u]);
 #pragma unroll
-                    for (int u = 0; u < U; ++u) {
-                        const int64_t c = c0 + u * G;
-                        if (c < nblk) {
-                            const int lo = c == 0 ? head : 0;
-                            const int hi = c == nblk - 1 ? tail : 8;
-#pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                v[u][j] = (j >= lo && j < hi) ? v[u][j] : ident;
+                    for (int u = 0; u < U; ++u)
+                        if (c0 + u * G < nfull)
                             f.chunk(v[u]);
-                        }
-                    }
                 }
+                f.scalar(hs);
+                f.scalar(ts);
+                f.pair(h2);
+                f.pair(t2);
+                f.quad(h4);
+                f.quad(t4);
             } else {
-                // a row in x's first or last partial 32-byte block
+                // the whole row inside one 32-byte block (fewer than 8 floats)
                 for (int64_t k = b + gl; k < e; k += G)
                     f.scalar(ld1(x + k));
             }

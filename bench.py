@@ -60,6 +60,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-stage-compare", action="store_true")
+    ap.add_argument("--no-supplementary", action="store_true",
+                    help="skip the 1 GiB row and column-product cases that grade the >= 1 GiB bars")
     ap.add_argument("--only", default="",
                     help="comma-separated op families to run (full1, full3, rows2, ragged5, colprod4a, "
                          "colprod4b); for profiling: the line is then not the benchmark's metric")
@@ -343,7 +345,7 @@ def run_ours(args):
         w.plan = [(name, key) for name, key in w.plan if name.split(" ")[0] in only]
         w.step_bytes = sum(w.bytes_of[k] for _, k in w.plan)
     if partial:
-        args.no_e2e = args.no_cpu_baseline = True
+        args.no_e2e = args.no_cpu_baseline = args.no_supplementary = True
         args.no_stage_compare = args.no_stage_compare or "full3" not in (only or ["full3"])
     calls = [(name, key, w.gpu_call(name)) for name, key in w.plan]
     torch.cuda.synchronize()
@@ -429,6 +431,9 @@ def run_ours(args):
     if not args.no_stage_compare:
         result["full_grid_stage_compare"] = compare_stages(w, stream)
 
+    if not args.no_supplementary:
+        result["supplementary_1gib"] = supplementary(stream, dev, peak)
+
     if not args.no_e2e:
         result["e2e"] = run_e2e(w, calls, stream, args.e2e_steps, world, dist, dev)
 
@@ -468,6 +473,49 @@ def compare_stages(w, stream, reps=10):
         out[label] = res
     itr.red_set_full_mode(keep)
     return {"unit": "GB/s", "note": "2^30 fp32, back-to-back calls (4 GiB > L2)", **out}
+
+
+def supplementary(stream, dev, peak, reps=10):
+    """The >= 1 GiB cases that grade the bandwidth bars of the row reductions
+    and the column products (not part of the step): 262144 x 1024 fp32 rows
+    (sum, max) and a 16384 x 16384 fp32 column product.  Back-to-back calls on
+    1 GiB inputs (> L2)."""
+    import torch
+    import int_tensor_reductions_gb300 as itr
+    from int_tensor_reductions_gb300 import synth
+    out = {"unit": "GB/s", "note": "1 GiB inputs, back-to-back calls, not part of the step"}
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    x = synth.normal((262144, 1024), 7, dev)
+    o = torch.empty(262144, device=dev)
+    nbytes = 4 * x.numel() + 4 * 262144
+    for op in ("sum", "max"):
+        ms = timed(lambda: itr.red_rows(op, x, out=o))
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[f"rows 262144x1024 {op}"] = {"gbs": round(gbs, 1), "frac_of_nominal_8TBs": round(gbs / NOMINAL_HBM_GBS, 4),
+                                         "frac_of_peak": round(gbs / peak, 4)}
+    del x, o
+    x = synth.uniform((16384, 16384), 0.999, 1.001, 8, dev)
+    o = torch.empty(16384, device=dev)
+    nbytes = 4 * x.numel() + 4 * 16384
+    ms = timed(lambda: itr.red_colprod(x, o))
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["colprod f32 16384x16384"] = {"gbs": round(gbs, 1), "frac_of_nominal_8TBs": round(gbs / NOMINAL_HBM_GBS, 4),
+                                      "frac_of_peak": round(gbs / peak, 4)}
+    del x, o
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(w, calls, stream, steps, world, dist, dev):

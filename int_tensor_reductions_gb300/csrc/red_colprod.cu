@@ -19,7 +19,7 @@
 namespace red {
 namespace {
 
-constexpr int CP_WY = 8;                 // warps per CTA (row interleave)
+constexpr int CP_WY = 16;                // warps per CTA (row interleave)
 constexpr int CP_NT = 32 * CP_WY;
 constexpr int CP_U = 4;                  // loads in flight per thread
 
@@ -162,22 +162,29 @@ int launch_cp(const T *x, int64_t R, int64_t C, T *out, cudaStream_t s, const De
     const int64_t tiles = (C + tile_cols - 1) / tile_cols;
     if (tiles > 0x7fffffffLL)
         return fail(RED_EINVAL, "red_colprod: C too large");
-    // Row splits: each warp keeps at least CP_U rows, and among those counts
-    // the one whose CTAs fill whole waves best.  With `slots` resident CTAs,
-    // s splits take ceil(tiles*s/slots) waves of R/s rows each, so minimise
-    // ceil(tiles*s/slots)/s (the smallest s on ties: fewer partials).
+    // Row splits: each warp keeps at least CP_U rows; among those counts take
+    // the smallest whose CTAs fill their waves of resident CTAs to at least
+    // 90% (more splits add partial-product traffic and per-CTA overhead),
+    // else the count with the best wave efficiency.
     int64_t splits = knob(RED_KNOB_COLPROD_SPLITS);
     if (splits <= 0) {
         const int64_t slots = (int64_t)di.sms * occ;
         int64_t smax = R / (CP_WY * CP_U);
         if (smax > 4096)
             smax = 4096;
+        if (smax < 1)
+            smax = 1;
         splits = 1;
-        double best = (double)((tiles + slots - 1) / slots);
-        for (int64_t sp = 2; sp <= smax; ++sp) {
-            const double t = (double)((tiles * sp + slots - 1) / slots) / (double)sp;
-            if (t < best * 0.999) {
-                best = t;
+        double best = -1.0;
+        for (int64_t sp = 1; sp <= smax; ++sp) {
+            const int64_t ctas = tiles * sp;
+            const double eff = (double)ctas / (double)(((ctas + slots - 1) / slots) * slots);
+            if (eff >= 0.9) {
+                splits = sp;
+                break;
+            }
+            if (eff > best) {
+                best = eff;
                 splits = sp;
             }
         }

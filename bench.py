@@ -432,6 +432,7 @@ def run_ours(args):
         result["full_grid_stage_compare"] = compare_stages(w, stream)
 
     if not args.no_supplementary:
+        result["fused_stats_2p30"] = fused_stats(w, stream, per_op)
         result["supplementary_1gib"] = supplementary(stream, dev, peak)
 
     if not args.no_e2e:
@@ -473,6 +474,27 @@ def compare_stages(w, stream, reps=10):
         out[label] = res
     itr.red_set_full_mode(keep)
     return {"unit": "GB/s", "note": "2^30 fp32, back-to-back calls (4 GiB > L2)", **out}
+
+
+def fused_stats(w, stream, per_op, reps=10):
+    """red_full_stats (sum, max, min, sum|x| from one read) on the 2^30 vector,
+    against the three separate red_full calls of the step."""
+    import torch
+    import int_tensor_reductions_gb300 as itr
+    out = torch.empty(4, device=w.x3.device)
+    for _ in range(2):
+        itr.red_full_stats(w.x3, out)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        itr.red_full_stats(w.x3, out)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    sep = sum(per_op[f"full3 {op}"]["ms"] for op in ("sum", "max", "min") if f"full3 {op}" in per_op)
+    return {"ms": round(ms, 4), "gbs": round(w.bytes_of["full3"] / (ms * 1e-3) / 1e9, 1),
+            "separate_sum_max_min_ms": round(sep, 4), "speedup_vs_separate": round(sep / ms, 3) if sep else None}
 
 
 def supplementary(stream, dev, peak, reps=10):

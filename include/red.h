@@ -103,6 +103,20 @@ enum red_knob {
 int red_full(int op, const float *x, int64_t n, float *out, red_stream_t stream);
 
 /*
+ * red_full_stats -- sum, max, min and sum of |x| of a 1-D fp32 vector from a
+ * single read of x (three red_full calls read it three times).  Each statistic
+ * is the one red_full computes ([TVM] "Algorithm": the packed-add sum fold
+ * and the max3 / min3 fold side by side in every thread); sum |x| is the sum
+ * of the absolute values (the scale of the sum's rounding error).
+ *   x      device pointer to n contiguous floats, n >= 1.
+ *   out    device pointer to 4 floats: out[0] = sum, out[1] = max,
+ *          out[2] = min, out[3] = sum of |x|.
+ * n == 0 returns RED_EINVAL (an empty vector has no max or min).  Uses the
+ * workspace (last-block grid stage) like red_full.
+ */
+int red_full_stats(const float *x, int64_t n, float *out, red_stream_t stream);
+
+/*
  * red_rows -- per-row reduction of a row-major fp32 matrix: row r is
  * x[r*len .. r*len+len), out[r] = op over row r.  With accum != 0 the old
  * value out[r] is folded in as one more operand ([TVM] "How inputs change the

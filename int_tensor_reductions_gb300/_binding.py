@@ -21,6 +21,7 @@ _i64, _int, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
 _SIGNATURES = {
     "red_full": ([_int, _vp, _i64, _vp, _vp], _int),
     "red_full_noalloc": ([_int, _vp, _i64, _vp, _vp], _int),
+    "red_full_stats": ([_vp, _i64, _vp, _vp], _int),
     "red_rows": ([_int, _vp, _i64, _i64, _int, _vp, _vp], _int),
     "red_rows_ragged": ([_int, _vp, _vp, _i64, _i64, _int, _vp, _vp], _int),
     "red_colprod": ([_int, _vp, _i64, _i64, _vp, _vp], _int),
@@ -102,6 +103,19 @@ def red_full(op, x: torch.Tensor, out: torch.Tensor | None = None, stream=None) 
     _need(out, "out", (torch.float32,))
     with torch.cuda.device(x.device):
         _check(lib().red_full(_op(op), x.data_ptr(), x.numel(), out.data_ptr(), _stream(stream, x.device)))
+    return out
+
+
+def red_full_stats(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Sum, max, min and sum |x| of fp32 ``x`` from one read, into ``out`` (shape (4,))."""
+    _need(x, "x", (torch.float32,))
+    if out is None:
+        out = torch.empty(4, dtype=torch.float32, device=x.device)
+    _need(out, "out", (torch.float32,))
+    if out.numel() < 4:
+        raise ValueError("out must hold 4 floats")
+    with torch.cuda.device(x.device):
+        _check(lib().red_full_stats(x.data_ptr(), x.numel(), out.data_ptr(), _stream(stream, x.device)))
     return out
 
 

@@ -153,6 +153,17 @@ int red_full(int op, const float *x, int64_t n, float *out, red_stream_t stream)
     return launch_full(op, x, n, out, s);
 }
 
+int red_full_stats(const float *x, int64_t n, float *out, red_stream_t stream)
+{
+    if (n <= 0 || n > MAX_ELEMS)
+        return fail(RED_EINVAL, "red_full_stats: n = %lld out of range (max/min need n >= 1)", (long long)n);
+    if (!out || misaligned(out, 4))
+        return fail(RED_EINVAL, "red_full_stats: out is NULL or not 4-byte aligned");
+    if (!x || misaligned(x, 4))
+        return fail(RED_EINVAL, "red_full_stats: x is NULL or not 4-byte aligned");
+    return launch_full_stats(x, n, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int red_rows(int op, const float *x, int64_t rows, int64_t len, int accum, float *out, red_stream_t stream)
 {
     if (op < RED_SUM || op > RED_MIN)

@@ -133,6 +133,25 @@ int red_rows(int op, const float *x, int64_t rows, int64_t len, int accum, float
              red_stream_t stream);
 
 /*
+ * red_rows_thread -- per-row reduction in which one GPU thread reduces each
+ * row with the thread-scope fold of [TVM] "Algorithm", exactly as the public
+ * device header red_device.cuh defines it (red_dev::thread_sum / thread_max /
+ * thread_min<len>): the row is the thread's register vector, and with accum
+ * the old out[r] is added into the fold's first accumulator slot ([TVM] "How
+ * inputs change the algorithm").  The rounding order of every row's sum is
+ * therefore fixed by len alone (the same bits on every GPU, grid and
+ * launch); red_rows is faster for long rows.  Row r is x[r*len ..
+ * r*len+len).
+ *   len    1 .. RED_THREAD_MAX_LEN (the register vector's static length; the
+ *          page's gate starts its packed fold at len 8, shorter rows fold
+ *          left to right).
+ *   other arguments as red_rows.  Invalid len returns RED_EINVAL.
+ */
+#define RED_THREAD_MAX_LEN 64
+int red_rows_thread(int op, const float *x, int64_t rows, int len, int accum, float *out,
+                    red_stream_t stream);
+
+/*
  * red_rows_ragged -- per-row reduction of packed rows of varying length:
  * row r is x[offsets[r] .. offsets[r+1]).  Same ops and accum as red_rows.
  *   x        device pointer to nnz floats.

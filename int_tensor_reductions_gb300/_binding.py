@@ -24,6 +24,7 @@ _SIGNATURES = {
     "red_full_stats": ([_vp, _i64, _vp, _vp], _int),
     "red_rows": ([_int, _vp, _i64, _i64, _int, _vp, _vp], _int),
     "red_rows_ragged": ([_int, _vp, _vp, _i64, _i64, _int, _vp, _vp], _int),
+    "red_rows_thread": ([_int, _vp, _i64, _int, _int, _vp, _vp], _int),
     "red_colprod": ([_int, _vp, _i64, _i64, _vp, _vp], _int),
     "red_set_full_mode": ([_int], _int),
     "red_get_full_mode": ([], _int),
@@ -149,6 +150,27 @@ def red_rows(op, x: torch.Tensor, accum: bool = False, out: torch.Tensor | None 
     with torch.cuda.device(x.device):
         _check(lib().red_rows(_op(op), x.data_ptr(), rows, length, int(bool(accum)), out.data_ptr(),
                               _stream(stream, x.device)))
+    return out
+
+
+def red_rows_thread(op, x: torch.Tensor, accum: bool = False, out: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """Per-row reduction of a (rows, len) fp32 matrix, len <= 64, one thread per
+    row with the page's thread-scope fold (fixed rounding order)."""
+    _need(x, "x", (torch.float32,))
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D (rows, len)")
+    rows, length = x.shape
+    if out is None:
+        if accum:
+            raise ValueError("accum needs an existing out")
+        out = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _need(out, "out", (torch.float32,))
+    if out.numel() != rows:
+        raise ValueError("out must have one element per row")
+    with torch.cuda.device(x.device):
+        _check(lib().red_rows_thread(_op(op), x.data_ptr(), rows, length, int(bool(accum)), out.data_ptr(),
+                                     _stream(stream, x.device)))
     return out
 
 

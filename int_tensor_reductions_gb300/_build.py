@@ -32,7 +32,8 @@ def _sources():
 
 def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
-        glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
+        glob.glob(os.path.join(INCLUDE, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.cuh")) + \
+        [os.path.abspath(__file__)]
 
 
 def is_stale() -> bool:

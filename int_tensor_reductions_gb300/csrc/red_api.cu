@@ -190,6 +190,23 @@ int red_rows(int op, const float *x, int64_t rows, int64_t len, int accum, float
     return launch_rows(op, x, rows, len, accum ? 1 : 0, out, s);
 }
 
+int red_rows_thread(int op, const float *x, int64_t rows, int len, int accum, float *out, red_stream_t stream)
+{
+    if (op < RED_SUM || op > RED_MIN)
+        return fail(RED_EINVAL, "red_rows_thread: unknown op %d", op);
+    if (len < 1 || len > RED_THREAD_MAX_LEN)
+        return fail(RED_EINVAL, "red_rows_thread: len = %d outside 1..%d", len, RED_THREAD_MAX_LEN);
+    if (rows < 0 || rows > MAX_ELEMS / len)
+        return fail(RED_EINVAL, "red_rows_thread: rows = %lld out of range", (long long)rows);
+    if (rows == 0)
+        return RED_OK;
+    if (!out || misaligned(out, 4))
+        return fail(RED_EINVAL, "red_rows_thread: out is NULL or not 4-byte aligned");
+    if (!x || misaligned(x, 4))
+        return fail(RED_EINVAL, "red_rows_thread: x is NULL or not 4-byte aligned");
+    return launch_rows_thread(op, x, rows, len, accum ? 1 : 0, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int red_rows_ragged(int op, const float *x, const int64_t *offsets, int64_t rows, int64_t nnz, int accum,
                     float *out, red_stream_t stream)
 {

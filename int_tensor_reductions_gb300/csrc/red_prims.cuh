@@ -21,38 +21,19 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "red_device.cuh"
+
 namespace red {
 
 enum : int { OP_SUM = 0, OP_MAX = 1, OP_MIN = 2 };
 
 // ------------------------------------------------------------ packed math
 
-__device__ __forceinline__ float2 add_f32x2(float2 a, float2 b)
-{
-    float2 d;
-    asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
-        "mov.b64 pa, {%2, %3};\n\t"
-        "mov.b64 pb, {%4, %5};\n\t"
-        "add.rn.ftz.f32x2 pd, pa, pb;\n\t"
-        "mov.b64 {%0, %1}, pd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-
-__device__ __forceinline__ float max3f(float a, float b, float c)
-{
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-
-__device__ __forceinline__ float min3f(float a, float b, float c)
-{
-    float d;
-    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
+// add.rn.ftz.f32x2 and the three-input max / min live in the public device
+// header (the thread-scope API); the kernels use the same instructions.
+__device__ __forceinline__ float2 add_f32x2(float2 a, float2 b) { return red_dev::add_f32x2(a, b); }
+__device__ __forceinline__ float max3f(float a, float b, float c) { return red_dev::max3(a, b, c); }
+__device__ __forceinline__ float min3f(float a, float b, float c) { return red_dev::min3(a, b, c); }
 
 __device__ __forceinline__ float add_ftz(float a, float b)
 {

@@ -1,0 +1,89 @@
+// red_thread.cu -- red_rows_thread: one thread per row, each row reduced by
+// the thread-scope fold of the public device header red_device.cuh (Apache
+// TVM docs, "reduction -> sm100_packed", "Algorithm"), so the rounding order
+// of every row's sum is the page's and depends on the row length alone.
+//
+// The row length is a template parameter (the register array of the fold
+// has a static size, like the page's local buffer), instantiated for
+// 1..RED_THREAD_MAX_LEN.  A CTA of 128 threads folds 128 consecutive rows;
+// their values (128 x len floats, contiguous) are staged through shared
+// memory with coalesced loads, at an odd row stride so that the threads'
+// row reads hit distinct banks, then each thread copies its row into
+// registers.
+#include "red_device.cuh"
+#include "red_internal.h"
+#include "red.h"
+
+namespace red {
+namespace {
+
+constexpr int TH_NT = 128;
+
+template <int OP, int N>
+__global__ void __launch_bounds__(TH_NT)
+thread_rows_kernel(const float *__restrict__ x, int64_t rows, int accum, float *__restrict__ out)
+{
+    constexpr int STRIDE = N | 1;  // odd row stride in shared memory
+    __shared__ float s_val[TH_NT * STRIDE];
+    const int64_t r0 = (int64_t)blockIdx.x * TH_NT;
+    const int nr = (int)((rows - r0) < TH_NT ? (rows - r0) : TH_NT);
+    const float *src = x + r0 * N;
+    for (int g = threadIdx.x; g < nr * N; g += TH_NT) {
+        const int t = g / N, i = g - t * N;
+        s_val[t * STRIDE + i] = __ldg(src + g);
+    }
+    __syncthreads();
+    if (threadIdx.x >= nr)
+        return;
+    float a[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+        a[i] = s_val[threadIdx.x * STRIDE + i];
+    const int64_t r = r0 + threadIdx.x;
+    const float old = accum ? out[r] : 0.0f;
+    float v;
+    if (OP == RED_SUM)
+        v = red_dev::thread_sum<N>(a, accum != 0, old);
+    else if (OP == RED_MAX)
+        v = red_dev::thread_max<N>(a, accum != 0, old);
+    else
+        v = red_dev::thread_min<N>(a, accum != 0, old);
+    out[r] = v;
+}
+
+template <int OP, int N>
+int launch_n(const float *x, int64_t rows, int accum, float *out, cudaStream_t s)
+{
+    const int64_t ctas = (rows + TH_NT - 1) / TH_NT;
+    if (ctas > 0x7fffffffLL)
+        return fail(RED_EINVAL, "red_rows_thread: too many rows");
+    thread_rows_kernel<OP, N><<<(unsigned)ctas, TH_NT, 0, s>>>(x, rows, accum, out);
+    count_launches(1);
+    return cuda_fail(cudaGetLastError(), "red_rows_thread launch");
+}
+
+// Dispatch a runtime length 1..RED_THREAD_MAX_LEN onto the instantiations.
+template <int OP, int N = 1>
+int dispatch(int len, const float *x, int64_t rows, int accum, float *out, cudaStream_t s)
+{
+    if constexpr (N > RED_THREAD_MAX_LEN) {
+        return fail(RED_EINVAL, "red_rows_thread: len %d out of range", len);
+    } else {
+        if (len == N)
+            return launch_n<OP, N>(x, rows, accum, out, s);
+        return dispatch<OP, N + 1>(len, x, rows, accum, out, s);
+    }
+}
+
+}  // namespace
+
+int launch_rows_thread(int op, const float *x, int64_t rows, int len, int accum, float *out, cudaStream_t s)
+{
+    switch (op) {
+    case RED_SUM: return dispatch<RED_SUM>(len, x, rows, accum, out, s);
+    case RED_MAX: return dispatch<RED_MAX>(len, x, rows, accum, out, s);
+    default: return dispatch<RED_MIN>(len, x, rows, accum, out, s);
+    }
+}
+
+}  // namespace red

@@ -59,6 +59,8 @@ def _load():
         "orc_colprod_f32": [vp, i64, i64, vp, vp],
         "orc_colprod_i32": [vp, i64, i64, vp],
     }
+    lib.orc_thread_sum.argtypes = [vp, i64, i32, ctypes.c_float]
+    lib.orc_thread_sum.restype = ctypes.c_float
     for name, args in sigs.items():
         fn = getattr(lib, name)
         fn.argtypes = args
@@ -178,6 +180,20 @@ def colprod_f32(x, R, C, out_f=None, want_double=False):
     out_d = np.zeros(C, np.float64) if want_double else None
     _check(_load().orc_colprod_f32(_ptr(x), R, C, _ptr(out_f), _ptr(out_d)), "colprod_f32")
     return (out_f, out_d) if want_double else out_f
+
+
+def thread_sum(a, accum=False, dst=0.0):
+    """The sm100_packed thread-scope sum of a 1-D vector in the page's fp32
+    rounding order (see orc_thread_sum in oracle.c); returns a float32."""
+    a = _f32(a).reshape(-1)
+    return np.float32(_load().orc_thread_sum(_ptr(a), a.size, int(bool(accum)), float(np.float32(dst))))
+
+
+def thread_rows_sum(x, rows, len_, accum=False, dst_old=None):
+    """thread_sum of every row of a row-major rows x len_ matrix (float32[rows])."""
+    x = _f32(x).reshape(rows, len_)
+    d = np.zeros(rows, np.float32) if dst_old is None else _f32(dst_old).reshape(-1)
+    return np.array([thread_sum(x[r], accum, d[r]) for r in range(rows)], np.float32)
 
 
 def colprod_i32(x, R, C, out=None):

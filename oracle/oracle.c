@@ -14,6 +14,10 @@
  *   - max / min compare the fp32 values directly (exact in any order);
  *   - fp32 column products accumulate in double and round to fp32 once;
  *   - int32 column products multiply in uint32, i.e. wrap modulo 2^32.
+ * One function is an algorithm rather than a definition: orc_thread_sum
+ * takes the steps of the sm100_packed thread-scope fold in the page's order,
+ * one fp32 operation each, so that a GPU fold in that order can be checked
+ * bit for bit (its result is the sum up to that fixed rounding order).
  *
  * Sources (cited by page title and section):
  *   [TVM]  Apache TVM docs, "reduction -> sm100_packed": sections "Algorithm"
@@ -33,7 +37,8 @@
  * Parity status: every function here is pinned by the CPU tests (page-given
  * 32-element check, closed forms, exact-arithmetic brute force, invariants).
  *
- * Return value of every function: 0 on success, -1 on invalid arguments.
+ * Return value of every function but orc_thread_sum: 0 on success, -1 on
+ * invalid arguments (orc_thread_sum returns the fp32 result).
  */
 #include <math.h>
 #include <stddef.h>
@@ -277,4 +282,51 @@ int orc_colprod_i32(const int32_t *x, int64_t R, int64_t C, int32_t *out)
         out[j] = (int32_t)p;
     }
     return ORC_OK;
+}
+
+/* ------------------------------------------------- thread-scope fold --- */
+
+/* [TVM] "Algorithm", sum (the sm100_packed thread-scope primitive), with
+ * the fp32 rounding order the page fixes, one fp32 operation per step:
+ *   n >= 8: s[0..7] = a[0..7]; with accum s[0] = s[0] + dst ("folds the old
+ *           dst value into the first accumulator slot"); every further full
+ *           chunk of 8 is added lane-wise, s[k] = s[k] + a[c+k]; a remainder
+ *           of r < 8 elements is added one at a time into slots 0..r-1
+ *           ("handle the remainder scalar"); then the 8 -> 4 -> 2 -> 1
+ *           collapse: (s0,s1) += (s2,s3), (s4,s5) += (s6,s7),
+ *           (s0,s1) += (s4,s5), result s0 + s1.
+ *   n < 8 (below the page's dispatch gate): a left-to-right fold starting
+ *           from a[0] (plus dst with accum).
+ * Only the order is the page's; each step is a plain fp32 round-to-nearest
+ * addition (no denormal can arise from the inputs used). */
+float orc_thread_sum(const float *a, int64_t n, int accum, float dst)
+{
+    if (n <= 0)
+        return accum ? dst : 0.0f;
+    if (n < 8) {
+        float r = a[0];
+        if (accum)
+            r = r + dst;
+        for (int64_t i = 1; i < n; ++i)
+            r = r + a[i];
+        return r;
+    }
+    float s[8];
+    for (int k = 0; k < 8; ++k)
+        s[k] = a[k];
+    if (accum)
+        s[0] = s[0] + dst;
+    int64_t c = 8;
+    for (; c + 8 <= n; c += 8)
+        for (int k = 0; k < 8; ++k)
+            s[k] = s[k] + a[c + k];
+    for (int64_t i = c; i < n; ++i)
+        s[i - c] = s[i - c] + a[i];
+    s[0] = s[0] + s[2];
+    s[1] = s[1] + s[3];
+    s[4] = s[4] + s[6];
+    s[5] = s[5] + s[7];
+    s[0] = s[0] + s[4];
+    s[1] = s[1] + s[5];
+    return s[0] + s[1];
 }

@@ -312,3 +312,41 @@ def test_colprod_i32_large_values_wrap():
     out = oracle.colprod_i32(x, R, C)
     for j in range(C):
         assert out[j] == _wrap32(math.prod(int(v) for v in x[:, j]))
+
+
+# ------------------------------------------------ thread-scope fold order
+
+def _fold_cases():
+    for name, accum, dst, expected, *vals in golden_lines("sm100_packed_fold_order.txt"):
+        yield name, bool(int(accum)), float(dst), float(expected), np.array([float(v) for v in vals], np.float32)
+
+
+def test_thread_sum_hand_worked_rounding_order():
+    """Apache TVM docs, "reduction -> sm100_packed", "Algorithm": the page's
+    fold order, worked by hand in fp32 (tests/golden/sm100_packed_fold_order.txt)."""
+    for name, accum, dst, expected, a in _fold_cases():
+        assert oracle.thread_sum(a, accum, dst) == np.float32(expected), name
+
+
+def test_thread_sum_page_demo():
+    """"Demonstration program": B == sum(A) for 32 float32 values."""
+    assert oracle.thread_sum(np.arange(32, dtype=np.float32)) == np.float32(496)
+
+
+@pytest.mark.parametrize("n", list(range(1, 65)))
+def test_thread_sum_exact_when_no_rounding(n):
+    """Integer values with small sums are exact in every order: closed form."""
+    a = np.arange(1, n + 1, dtype=np.float32)
+    assert oracle.thread_sum(a) == np.float32(n * (n + 1) // 2)
+    assert oracle.thread_sum(a, True, 7.0) == np.float32(n * (n + 1) // 2 + 7)
+
+
+def test_thread_sum_within_the_fp32_error_bound():
+    """Random data: |fold - exact| <= (n - 1) * 2**-24 * sum|a| (any fp32
+    summation order of n terms satisfies this)."""
+    rng = np.random.default_rng(31)
+    for n in range(1, 65):
+        a = _grid_uniform(rng, n, -4.0, 4.0)
+        exact = math.fsum(float(v) for v in a)
+        bound = max(n - 1, 1) * 2.0**-24 * math.fsum(abs(float(v)) for v in a)
+        assert abs(float(oracle.thread_sum(a)) - exact) <= bound, n

@@ -61,6 +61,12 @@ def _load():
     }
     lib.orc_thread_sum.argtypes = [vp, i64, i32, ctypes.c_float]
     lib.orc_thread_sum.restype = ctypes.c_float
+    lib.orc_half_to_double.argtypes = [ctypes.c_uint16]
+    lib.orc_half_to_double.restype = ctypes.c_double
+    lib.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
+    lib.orc_bf16_to_double.restype = ctypes.c_double
+    sigs["orc_cols_f"] = [i32, i32, vp, i64, i64, vp, vp]
+    sigs["orc_cols_i"] = [i32, i32, vp, i64, i64, vp]
     for name, args in sigs.items():
         fn = getattr(lib, name)
         fn.argtypes = args
@@ -205,3 +211,41 @@ def colprod_i32(x, R, C, out=None):
         out = np.zeros(C, np.int32)
     _check(_load().orc_colprod_i32(_ptr(x), R, C, _ptr(out)), "colprod_i32")
     return out
+
+
+# ---------------------------------------------------- column reductions
+
+COL_DTYPES = {"f32": 0, "i32": 1, "f16": 2, "bf16": 3, "i16": 4, "u16": 5, "u32": 6}
+COL_OPS = {"sum": 0, "max": 1, "min": 2, "prod": 3}
+_COL_BYTES = {"f32": 4, "i32": 4, "u32": 4, "f16": 2, "bf16": 2, "i16": 2, "u16": 2}
+
+
+def half_to_double(bits: int) -> float:
+    return _load().orc_half_to_double(int(bits) & 0xFFFF)
+
+
+def bf16_to_double(bits: int) -> float:
+    return _load().orc_bf16_to_double(int(bits) & 0xFFFF)
+
+
+def cols(op, dtype, x, R, C, out=None):
+    """Column reductions of a row-major R x C matrix given as raw element
+    storage (any numpy array whose bytes are the R*C elements of ``dtype``).
+
+    Floating types return (float64[C] result, float64[C] sum|x|); integer
+    types return int64[C] (the result as the type, sign-extended).  With
+    R == 0 or C == 0 the oracle returns early: ``out`` (if given) is left as
+    it is and returned.
+    """
+    raw = np.ascontiguousarray(x).view(np.uint8).reshape(-1)
+    if raw.size != R * C * _COL_BYTES[dtype]:
+        raise OracleError("x has the wrong size")
+    lib = _load()
+    if dtype in ("f32", "f16", "bf16"):
+        res = np.zeros(C, np.float64) if out is None else out
+        ab = np.zeros(C, np.float64)
+        _check(lib.orc_cols_f(COL_OPS[op], COL_DTYPES[dtype], _ptr(raw), R, C, _ptr(res), _ptr(ab)), "cols_f")
+        return res, ab
+    res = np.zeros(C, np.int64) if out is None else out
+    _check(lib.orc_cols_i(COL_OPS[op], COL_DTYPES[dtype], _ptr(raw), R, C, _ptr(res)), "cols_i")
+    return res

@@ -43,6 +43,7 @@
 #include <math.h>
 #include <stddef.h>
 #include <stdint.h>
+#include <string.h>
 
 #define ORC_OK 0
 #define ORC_EINVAL (-1)
@@ -329,4 +330,142 @@ float orc_thread_sum(const float *a, int64_t n, int accum, float dst)
     s[0] = s[0] + s[4];
     s[1] = s[1] + s[5];
     return s[0] + s[1];
+}
+
+/* ------------------------------------------------ column reductions --- */
+
+/* Element types (the A2A3 / A5 lists of pto-isa docs, "TCOLPROD",
+ * "Constraints"): 0 float, 1 int32, 2 half, 3 bfloat16, 4 int16,
+ * 5 uint16, 6 uint32.  Operators: 0 sum, 1 max, 2 min, 3 product. */
+enum { ORC_F32 = 0, ORC_I32 = 1, ORC_F16 = 2, ORC_BF16 = 3, ORC_I16 = 4, ORC_U16 = 5, ORC_U32 = 6 };
+enum { ORC_SUM = 0, ORC_MAX = 1, ORC_MIN = 2, ORC_PROD = 3 };
+
+/* IEEE binary16 bits -> double, exactly (sign, 5-bit exponent, 10-bit
+ * fraction; subnormals, infinities and NaN included). */
+double orc_half_to_double(uint16_t h)
+{
+    const int sign = h >> 15, e = (h >> 10) & 0x1f, f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);                 /* subnormal: f * 2^-24 */
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(f | 0x400), e - 25);    /* (1024 + f) * 2^(e-25) */
+    return sign ? -v : v;
+}
+
+/* bfloat16 bits -> double, exactly: the high half of a binary32. */
+double orc_bf16_to_double(uint16_t b)
+{
+    const uint32_t w = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+static int elem_size(int dtype)
+{
+    switch (dtype) {
+    case ORC_F32: case ORC_I32: case ORC_U32: return 4;
+    case ORC_F16: case ORC_BF16: case ORC_I16: case ORC_U16: return 2;
+    default: return 0;
+    }
+}
+
+static double elem_f(const void *x, int dtype, int64_t k)
+{
+    switch (dtype) {
+    case ORC_F32: return (double)((const float *)x)[k];
+    case ORC_F16: return orc_half_to_double(((const uint16_t *)x)[k]);
+    default: return orc_bf16_to_double(((const uint16_t *)x)[k]);
+    }
+}
+
+static int64_t elem_i(const void *x, int dtype, int64_t k)
+{
+    switch (dtype) {
+    case ORC_I32: return (int64_t)((const int32_t *)x)[k];
+    case ORC_U32: return (int64_t)((const uint32_t *)x)[k];
+    case ORC_I16: return (int64_t)((const int16_t *)x)[k];
+    default: return (int64_t)((const uint16_t *)x)[k];
+    }
+}
+
+/* Column reductions of a row-major R x C matrix of a floating type:
+ * out[j] = op over rows i of x[i][j] in double (sum and product accumulate
+ * in index order; max / min compare directly), abs_out[j] (may be NULL) =
+ * sum of |x[i][j]|.  R == 0 or C == 0 returns early, writing nothing (the
+ * TCOLPROD rule, applied to the column siblings as well). */
+int orc_cols_f(int op, int dtype, const void *x, int64_t R, int64_t C, double *out, double *abs_out)
+{
+    if (op < ORC_SUM || op > ORC_PROD || !(dtype == ORC_F32 || dtype == ORC_F16 || dtype == ORC_BF16) ||
+        R < 0 || C < 0)
+        return ORC_EINVAL;
+    if (R == 0 || C == 0)
+        return ORC_OK;
+    if (!x || !out)
+        return ORC_EINVAL;
+    for (int64_t j = 0; j < C; ++j) {
+        double acc = elem_f(x, dtype, j), a = fabs(acc);
+        for (int64_t i = 1; i < R; ++i) {
+            const double v = elem_f(x, dtype, i * C + j);
+            a += fabs(v);
+            if (op == ORC_SUM)
+                acc += v;
+            else if (op == ORC_PROD)
+                acc *= v;
+            else if (op == ORC_MAX)
+                acc = v > acc ? v : acc;
+            else
+                acc = v < acc ? v : acc;
+        }
+        out[j] = acc;
+        if (abs_out)
+            abs_out[j] = a;
+    }
+    return ORC_OK;
+}
+
+/* The same for an integer type: sum and product wrap modulo 2^bits of the
+ * type (done in uint64, then reduced to the type's width and read back as
+ * the type, so signed results are two's complement); max / min compare the
+ * values.  out[j] holds the result as a (sign-extended) int64. */
+int orc_cols_i(int op, int dtype, const void *x, int64_t R, int64_t C, int64_t *out)
+{
+    if (op < ORC_SUM || op > ORC_PROD || !(dtype == ORC_I32 || dtype == ORC_U32 || dtype == ORC_I16 ||
+                                           dtype == ORC_U16) ||
+        R < 0 || C < 0)
+        return ORC_EINVAL;
+    if (R == 0 || C == 0)
+        return ORC_OK;
+    if (!x || !out)
+        return ORC_EINVAL;
+    const int bits = 8 * elem_size(dtype);
+    const uint64_t mask = bits == 64 ? ~0ull : ((1ull << bits) - 1);
+    const int is_signed = dtype == ORC_I32 || dtype == ORC_I16;
+    for (int64_t j = 0; j < C; ++j) {
+        int64_t m = elem_i(x, dtype, j);
+        uint64_t w = (uint64_t)m;
+        for (int64_t i = 1; i < R; ++i) {
+            const int64_t v = elem_i(x, dtype, i * C + j);
+            if (op == ORC_SUM)
+                w += (uint64_t)v;
+            else if (op == ORC_PROD)
+                w *= (uint64_t)v;
+            else if (op == ORC_MAX)
+                m = v > m ? v : m;
+            else
+                m = v < m ? v : m;
+        }
+        if (op == ORC_SUM || op == ORC_PROD) {
+            w &= mask;
+            if (is_signed && (w >> (bits - 1)) & 1u)
+                m = (int64_t)w - (int64_t)(mask + 1);
+            else
+                m = (int64_t)w;
+        }
+        out[j] = m;
+    }
+    return ORC_OK;
 }

@@ -350,3 +350,111 @@ def test_thread_sum_within_the_fp32_error_bound():
         exact = math.fsum(float(v) for v in a)
         bound = max(n - 1, 1) * 2.0**-24 * math.fsum(abs(float(v)) for v in a)
         assert abs(float(oracle.thread_sum(a)) - exact) <= bound, n
+
+
+# ------------------------------------------------ column reductions, all types
+
+def test_half_decode_exhaustive():
+    """Every binary16 bit pattern decodes as numpy's float16 does."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    got = np.array([oracle.half_to_double(int(b)) for b in bits])
+    same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    assert same.all()
+
+
+def test_bf16_decode_exhaustive():
+    """Every bfloat16 bit pattern decodes as torch's bfloat16 does."""
+    import torch
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([oracle.bf16_to_double(int(b)) for b in bits])
+    same = (got == ref) | (np.isnan(got) & np.isnan(ref))
+    assert same.all()
+
+
+def _wrap(v, bits, signed):
+    v %= 1 << bits
+    return v - (1 << bits) if signed and v >= 1 << (bits - 1) else v
+
+
+@pytest.mark.parametrize("dtype,bits,signed", [("i32", 32, True), ("u32", 32, False), ("i16", 16, True),
+                                               ("u16", 16, False)])
+def test_int_cols_bruteforce(dtype, bits, signed):
+    rng = np.random.default_rng(bits + signed)
+    npt = {"i32": np.int32, "u32": np.uint32, "i16": np.int16, "u16": np.uint16}[dtype]
+    info = np.iinfo(npt)
+    for R, C in [(1, 3), (5, 4), (17, 6), (64, 3)]:
+        x = rng.integers(int(info.min), int(info.max) + 1, size=(R, C), dtype=np.int64).astype(npt)
+        for op in ("sum", "prod", "max", "min"):
+            got = oracle.cols(op, dtype, x, R, C)
+            for j in range(C):
+                col = [int(v) for v in x[:, j]]
+                if op == "sum":
+                    ref = _wrap(sum(col), bits, signed)
+                elif op == "prod":
+                    ref = _wrap(math.prod(col), bits, signed)
+                else:
+                    ref = max(col) if op == "max" else min(col)
+                assert got[j] == ref, (dtype, op, R, C, j)
+
+
+def test_int16_wrap_closed_forms():
+    """2^15 wraps to -32768 in int16 and 2^16 to 0; 3^11 = 177147 wraps to
+    177147 - 3 * 65536 = -19461; the unsigned types wrap to the residue."""
+    for c, R, dtype, ref in [(2, 15, "i16", -32768), (2, 16, "i16", 0), (3, 11, "i16", 177147 - 3 * 65536),
+                             (3, 11, "u16", 177147 % 65536), (2, 32, "u32", 0), (3, 21, "u32", 3**21 % 2**32),
+                             (-1, 7, "i16", -1)]:
+        npt = {"i16": np.int16, "u16": np.uint16, "u32": np.uint32}[dtype]
+        x = np.full((R, 2), c, np.int64).astype(npt)
+        assert (oracle.cols("prod", dtype, x, R, 2) == ref).all(), (c, R, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_float_cols_bruteforce(dtype):
+    import torch
+    rng = np.random.default_rng(5)
+    for R, C in [(1, 2), (3, 5), (16, 16), (40, 3)]:
+        v = rng.uniform(0.5, 1.5, size=(R, C)).astype(np.float32)
+        if dtype == "f32":
+            x = v
+            vals = v.astype(np.float64)
+        elif dtype == "f16":
+            x = v.astype(np.float16)
+            vals = x.astype(np.float64)
+        else:
+            t = torch.from_numpy(v).to(torch.bfloat16)
+            x = t.view(torch.int16).numpy()
+            vals = t.to(torch.float64).numpy()
+        for op in ("sum", "prod", "max", "min"):
+            got, ab = oracle.cols(op, dtype, x, R, C)
+            for j in range(C):
+                col = [float(a) for a in vals[:, j]]
+                assert ab[j] == math.fsum(abs(a) for a in col)
+                if op == "sum":
+                    assert got[j] == math.fsum(col)           # exact: few short values
+                elif op == "prod":
+                    ex = math.prod(Fraction(a) for a in col)
+                    assert abs(Fraction(got[j]) - ex) <= abs(ex) * R * Fraction(2) ** -53
+                else:
+                    assert got[j] == (max(col) if op == "max" else min(col))
+
+
+def test_cols_not_transposed_and_early_return():
+    x = np.array([[1, 2, 3], [4, 5, 6]], np.int32)
+    assert oracle.cols("sum", "i32", x, 2, 3).tolist() == [5, 7, 9]
+    assert oracle.cols("prod", "i32", x, 2, 3).tolist() == [4, 10, 18]
+    sentinel = np.full(3, 7, np.int64)
+    oracle.cols("sum", "i32", np.zeros((0, 3), np.int32), 0, 3, out=sentinel)
+    assert sentinel.tolist() == [7, 7, 7]
+    fs = np.full(3, 2.5)
+    oracle.cols("max", "f16", np.zeros((0, 3), np.float16), 0, 3, out=fs)
+    assert fs.tolist() == [2.5, 2.5, 2.5]
+
+
+def test_cols_f32_product_matches_colprod():
+    rng = np.random.default_rng(6)
+    x = rng.uniform(0.9, 1.1, size=(30, 7)).astype(np.float32)
+    got, _ = oracle.cols("prod", "f32", x, 30, 7)
+    _, pd = oracle.colprod_f32(x, 30, 7, want_double=True)
+    assert (got == pd).all()

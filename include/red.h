@@ -63,11 +63,21 @@ extern "C" {
 /* The same type as cudaStream_t. */
 typedef struct CUstream_st *red_stream_t;
 
-/* Reduction operator. */
-enum red_op { RED_SUM = 0, RED_MAX = 1, RED_MIN = 2 };
+/* Reduction operator.  RED_PROD is accepted by the column reductions only. */
+enum red_op { RED_SUM = 0, RED_MAX = 1, RED_MIN = 2, RED_PROD = 3 };
 
-/* Element type of red_colprod. */
-enum red_dtype { RED_F32 = 0, RED_I32 = 1 };
+/* Element type of the column reductions (red_cols, red_colprod): float,
+ * int32, IEEE binary16, bfloat16, int16, uint16, uint32 -- the element types
+ * of [PTO] "A2A3 implementation checks" and "A5 implementation checks". */
+enum red_dtype {
+    RED_F32 = 0,
+    RED_I32 = 1,
+    RED_F16 = 2,
+    RED_BF16 = 3,
+    RED_I16 = 4,
+    RED_U16 = 5,
+    RED_U32 = 6
+};
 
 /* Status codes. */
 enum red_status { RED_OK = 0, RED_EINVAL = -1, RED_ECUDA = -2, RED_ENOMEM = -3 };
@@ -84,7 +94,7 @@ enum red_full_mode {
 enum red_knob {
     RED_KNOB_ROWS_GROUP = 1,   /* lanes per dense row: 1, 2, 4, 8, 16 or 32 */
     RED_KNOB_RAGGED_GROUP = 2, /* lanes per ragged row: 1, 2, 4, 8, 16 or 32 */
-    RED_KNOB_COLPROD_SPLITS = 3, /* CTAs along the row axis of red_colprod (>= 1) */
+    RED_KNOB_COLPROD_SPLITS = 3, /* CTAs along the row axis of red_cols / red_colprod (>= 1) */
     RED_KNOB_FULL_CTAS_PER_SM = 4 /* resident CTAs per SM for red_full (>= 1) */
 };
 
@@ -170,13 +180,32 @@ int red_rows_ragged(int op, const float *x, const int64_t *offsets, int64_t rows
                     int accum, float *out, red_stream_t stream);
 
 /*
- * red_colprod -- [PTO] TCOLPROD: out[j] = prod_{i=0}^{R-1} x[i*C + j] for
- * 0 <= j < C, x row-major R x C.
- *   dtype  RED_F32 (fp32 products, round-to-nearest) or RED_I32 (int32
- *          products wrapping modulo 2^32); x and out have this type.
- *   x      device pointer to R*C elements.   out  device pointer to C elements.
- *   R, C   >= 0.  R == 0 or C == 0 returns RED_OK at once and writes nothing
- *          ([PTO] "Constraints": the implementation returns early).
+ * red_cols -- column reductions of a row-major R x C matrix:
+ * out[j] = op_{i=0}^{R-1} x[i*C + j] for 0 <= j < C.  op RED_PROD is [PTO]
+ * TCOLPROD ("Math Interpretation"); RED_SUM, RED_MAX and RED_MIN are its
+ * column siblings over the same layout.  x and out have the element type
+ * `dtype` ([PTO] "Constraints": the same element type on both sides).
+ *   Arithmetic: floating types accumulate in fp32 (RED_F16 / RED_BF16 are
+ *   widened exactly and the result is rounded to nearest-even once; products
+ *   and sums use round-to-nearest fp32 steps, so an fp32 product of R values
+ *   is within about R * 2^-24 relative of the exact product); integer sums
+ *   and products wrap modulo 2^bits of the type; max / min compare values
+ *   (signed for RED_I32 / RED_I16, unsigned for RED_U32 / RED_U16; NaN
+ *   inputs are not supported).
+ *   x, out  device pointers aligned to the element size; out holds C elements.
+ *   R, C    >= 0.  R == 0 or C == 0 returns RED_OK at once and writes nothing
+ *           ([PTO] "Constraints": the implementation returns early; the same
+ *           rule is kept for the siblings).
+ * Bad op or dtype, negative sizes, NULL or misaligned pointers: RED_EINVAL.
+ */
+int red_cols(int op, int dtype, const void *x, int64_t R, int64_t C, void *out, red_stream_t stream);
+
+/*
+ * red_colprod -- [PTO] TCOLPROD: red_cols(RED_PROD, dtype, ...).
+ *   dtype  any enum red_dtype; RED_F32 products round to nearest in fp32,
+ *          RED_I32 (and the other integer types) wrap modulo 2^bits.
+ *   R == 0 or C == 0 returns RED_OK at once and writes nothing ([PTO]
+ *   "Constraints": the implementation returns early).
  */
 int red_colprod(int dtype, const void *x, int64_t R, int64_t C, void *out, red_stream_t stream);
 

@@ -6,13 +6,21 @@ import os
 
 import torch
 
-RED_SUM, RED_MAX, RED_MIN = 0, 1, 2
-RED_F32, RED_I32 = 0, 1
+RED_SUM, RED_MAX, RED_MIN, RED_PROD = 0, 1, 2, 3
+RED_F32, RED_I32, RED_F16, RED_BF16, RED_I16, RED_U16, RED_U32 = 0, 1, 2, 3, 4, 5, 6
 RED_OK, RED_EINVAL, RED_ECUDA, RED_ENOMEM = 0, -1, -2, -3
 RED_MODE_AUTO, RED_MODE_TWO_PASS, RED_MODE_LAST_BLOCK, RED_MODE_ATOMIC = 0, 1, 2, 3
 RED_KNOB_ROWS_GROUP, RED_KNOB_RAGGED_GROUP, RED_KNOB_COLPROD_SPLITS, RED_KNOB_FULL_CTAS_PER_SM = 1, 2, 3, 4
 
-_OPS = {"sum": RED_SUM, "max": RED_MAX, "min": RED_MIN}
+_OPS = {"sum": RED_SUM, "max": RED_MAX, "min": RED_MIN, "prod": RED_PROD}
+# element type names of the column reductions and their sizes in bytes
+_COL_DTYPES = {"f32": (RED_F32, 4), "i32": (RED_I32, 4), "f16": (RED_F16, 2), "bf16": (RED_BF16, 2),
+               "i16": (RED_I16, 2), "u16": (RED_U16, 2), "u32": (RED_U32, 4)}
+_TORCH_COL = {torch.float32: "f32", torch.int32: "i32", torch.float16: "f16", torch.bfloat16: "bf16",
+              torch.int16: "i16"}
+for _name, _key in (("uint16", "u16"), ("uint32", "u32")):
+    if hasattr(torch, _name):
+        _TORCH_COL[getattr(torch, _name)] = _key
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libred.so")
 _lib = None
@@ -26,6 +34,7 @@ _SIGNATURES = {
     "red_rows_ragged": ([_int, _vp, _vp, _i64, _i64, _int, _vp, _vp], _int),
     "red_rows_thread": ([_int, _vp, _i64, _int, _int, _vp, _vp], _int),
     "red_colprod": ([_int, _vp, _i64, _i64, _vp, _vp], _int),
+    "red_cols": ([_int, _int, _vp, _i64, _i64, _vp, _vp], _int),
     "red_set_full_mode": ([_int], _int),
     "red_get_full_mode": ([], _int),
     "red_set_knob": ([_int, _int], _int),
@@ -195,20 +204,55 @@ def red_rows_ragged(op, x: torch.Tensor, offsets: torch.Tensor, accum: bool = Fa
     return out
 
 
-def red_colprod(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """TCOLPROD: out[j] = prod_i x[i, j] for a (R, C) fp32 or int32 matrix."""
-    _need(x, "x", (torch.float32, torch.int32))
+def _col_dtype(x: torch.Tensor, dtype):
+    key = dtype if dtype is not None else _TORCH_COL.get(x.dtype)
+    if key not in _COL_DTYPES:
+        raise ValueError(f"unsupported element type {x.dtype if dtype is None else dtype}")
+    code, size = _COL_DTYPES[key]
+    if x.element_size() != size:
+        raise ValueError(f"element type {key} needs {size}-byte elements, x has {x.element_size()}")
+    return code
+
+
+def red_cols(op, x: torch.Tensor, out: torch.Tensor | None = None, stream=None, dtype=None) -> torch.Tensor:
+    """Column reduction out[j] = op_i x[i, j] (op "sum", "max", "min" or
+    "prod") of a (R, C) matrix of float32, int32, float16, bfloat16, int16,
+    uint16 or uint32; ``dtype`` ("u16", "u32", ...) reads x's storage as that
+    element type (same element size), e.g. int16 storage as uint16."""
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor")
     if x.dim() != 2:
         raise ValueError("x must be 2-D (R, C)")
+    code = _col_dtype(x, dtype)
     R, C = x.shape
     if out is None:
         out = torch.empty(C, dtype=x.dtype, device=x.device)
-    _need(out, "out", (x.dtype,))
+    if not out.is_cuda or not out.is_contiguous() or out.element_size() != x.element_size():
+        raise ValueError("out must be a contiguous CUDA tensor of x's element size")
     if out.numel() != C:
         raise ValueError("out must have C elements")
-    dtype = RED_F32 if x.dtype == torch.float32 else RED_I32
     with torch.cuda.device(x.device):
-        _check(lib().red_colprod(dtype, x.data_ptr(), R, C, out.data_ptr(), _stream(stream, x.device)))
+        _check(lib().red_cols(_op(op), code, x.data_ptr(), R, C, out.data_ptr(), _stream(stream, x.device)))
+    return out
+
+
+def red_colprod(x: torch.Tensor, out: torch.Tensor | None = None, stream=None, dtype=None) -> torch.Tensor:
+    """TCOLPROD: out[j] = prod_i x[i, j] for a (R, C) matrix of any element
+    type red_cols accepts (float32 rounds per step, integers wrap)."""
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor")
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D (R, C)")
+    code = _col_dtype(x, dtype)
+    R, C = x.shape
+    if out is None:
+        out = torch.empty(C, dtype=x.dtype, device=x.device)
+    if not out.is_cuda or not out.is_contiguous() or out.element_size() != x.element_size():
+        raise ValueError("out must be a contiguous CUDA tensor of x's element size")
+    if out.numel() != C:
+        raise ValueError("out must have C elements")
+    with torch.cuda.device(x.device):
+        _check(lib().red_colprod(code, x.data_ptr(), R, C, out.data_ptr(), _stream(stream, x.device)))
     return out
 
 

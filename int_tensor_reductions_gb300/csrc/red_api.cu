@@ -227,19 +227,29 @@ int red_rows_ragged(int op, const float *x, const int64_t *offsets, int64_t rows
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
-int red_colprod(int dtype, const void *x, int64_t R, int64_t C, void *out, red_stream_t stream)
+int red_cols(int op, int dtype, const void *x, int64_t R, int64_t C, void *out, red_stream_t stream)
 {
-    if (dtype != RED_F32 && dtype != RED_I32)
-        return fail(RED_EINVAL, "red_colprod: unknown dtype %d", dtype);
+    if (op < RED_SUM || op > RED_PROD)
+        return fail(RED_EINVAL, "red_cols: unknown op %d", op);
+    if (dtype < RED_F32 || dtype > RED_U32)
+        return fail(RED_EINVAL, "red_cols: unknown dtype %d", dtype);
     if (R < 0 || C < 0 || R > MAX_ELEMS || C > MAX_ELEMS || (C > 0 && R > MAX_ELEMS / C))
-        return fail(RED_EINVAL, "red_colprod: R = %lld, C = %lld out of range", (long long)R, (long long)C);
+        return fail(RED_EINVAL, "red_cols: R = %lld, C = %lld out of range", (long long)R, (long long)C);
     if (R == 0 || C == 0)
         return RED_OK;  // TCOLPROD returns early on an empty tile; dst untouched
-    if (!x || misaligned(x, 4))
-        return fail(RED_EINVAL, "red_colprod: x is NULL or not 4-byte aligned");
-    if (!out || misaligned(out, 4))
-        return fail(RED_EINVAL, "red_colprod: out is NULL or not 4-byte aligned");
-    return launch_colprod(dtype, x, R, C, out, reinterpret_cast<cudaStream_t>(stream));
+    const uintptr_t esz = (dtype == RED_F32 || dtype == RED_I32 || dtype == RED_U32) ? 4 : 2;
+    if (!x || misaligned(x, esz))
+        return fail(RED_EINVAL, "red_cols: x is NULL or not aligned to its element size");
+    if (!out || misaligned(out, esz))
+        return fail(RED_EINVAL, "red_cols: out is NULL or not aligned to its element size");
+    return launch_cols(op, dtype, x, R, C, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int red_colprod(int dtype, const void *x, int64_t R, int64_t C, void *out, red_stream_t stream)
+{
+    if (dtype < RED_F32 || dtype > RED_U32)
+        return fail(RED_EINVAL, "red_colprod: unknown dtype %d", dtype);
+    return red_cols(RED_PROD, dtype, x, R, C, out, stream);
 }
 
 int red_set_full_mode(int mode)

@@ -1,0 +1,395 @@
+// red_cols.cu -- column reductions dst[0,j] = op_{i<R} src[i,j] of a row-major
+// R x C matrix: TCOLPROD (pto-isa docs, "TCOLPROD", "Math Interpretation")
+// and its column siblings sum, max and min, for the element types of that
+// page's A2A3 / A5 lists ("Constraints"): float, int32, half, bfloat16,
+// int16, uint16, uint32.  dst has src's element type.
+//
+// Arithmetic: floating types accumulate in fp32 (products __fmul_rn, sums
+// __fadd_rn; half and bfloat16 are widened exactly and the result is rounded
+// to nearest once); integer sums and products wrap modulo 2^bits of the type
+// (done in 32-bit unsigned arithmetic, then truncated for the 16-bit types);
+// max / min compare values (signed or unsigned as the type is).
+//
+// Layout of the work: a CTA owns a tile of 32*V adjacent columns and 16
+// warps.  Lane l of every warp owns V adjacent columns of the tile and keeps
+// V running accumulators (per-thread column accumulators); warp w walks rows
+// i0+w, i0+w+16, ... of the CTA's row slab, so each warp reads 32 bytes per
+// lane of a row per load (coalesced, row-major order kept).  The 16 warp
+// results meet in shared memory (fixed order).  gridDim.y CTAs split the
+// rows; with more than one, the CTA partials go to the workspace and the CTA
+// that arrives last for its column tile folds them (in split order) into
+// dst.  No CTA ever waits for another.
+#include "red_internal.h"
+#include "red_prims.cuh"
+#include "red.h"
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace red {
+namespace {
+
+constexpr int CP_WY = 16;                // warps per CTA (row interleave)
+constexpr int CP_NT = 32 * CP_WY;
+
+// ------------------------------------------------------- element types
+
+template <int DT>
+struct Elem;
+
+template <>
+struct Elem<RED_F32> {
+    using T = float;
+    using A = float;
+    static __device__ __forceinline__ A widen(uint32_t bits) { return __uint_as_float(bits); }
+    static __device__ __forceinline__ T narrow(A a) { return a; }
+};
+template <>
+struct Elem<RED_I32> {
+    using T = int32_t;
+    using A = int32_t;
+    static __device__ __forceinline__ A widen(uint32_t bits) { return (int32_t)bits; }
+    static __device__ __forceinline__ T narrow(A a) { return a; }
+};
+template <>
+struct Elem<RED_U32> {
+    using T = uint32_t;
+    using A = uint32_t;
+    static __device__ __forceinline__ A widen(uint32_t bits) { return bits; }
+    static __device__ __forceinline__ T narrow(A a) { return a; }
+};
+template <>
+struct Elem<RED_F16> {
+    using T = uint16_t;  // binary16 bits
+    using A = float;
+    static __device__ __forceinline__ A widen(uint32_t bits)
+    {
+        return __half2float(__ushort_as_half((unsigned short)bits));
+    }
+    static __device__ __forceinline__ T narrow(A a) { return __half_as_ushort(__float2half_rn(a)); }
+};
+template <>
+struct Elem<RED_BF16> {
+    using T = uint16_t;  // bfloat16 bits
+    using A = float;
+    static __device__ __forceinline__ A widen(uint32_t bits) { return __uint_as_float(bits << 16); }
+    static __device__ __forceinline__ T narrow(A a) { return __bfloat16_as_ushort(__float2bfloat16_rn(a)); }
+};
+template <>
+struct Elem<RED_I16> {
+    using T = int16_t;
+    using A = int32_t;
+    static __device__ __forceinline__ A widen(uint32_t bits) { return (int32_t)(int16_t)(uint16_t)bits; }
+    static __device__ __forceinline__ T narrow(A a) { return (int16_t)(uint16_t)(uint32_t)a; }
+};
+template <>
+struct Elem<RED_U16> {
+    using T = uint16_t;
+    using A = uint32_t;
+    static __device__ __forceinline__ A widen(uint32_t bits) { return bits & 0xffffu; }
+    static __device__ __forceinline__ T narrow(A a) { return (uint16_t)a; }
+};
+
+// ------------------------------------------------------------ operators
+
+template <int OP, typename A>
+struct Comb;
+
+template <int OP>
+struct Comb<OP, float> {
+    static __device__ __forceinline__ float identity()
+    {
+        return OP == RED_SUM ? 0.0f
+                             : OP == RED_PROD ? 1.0f
+                                              : OP == RED_MAX ? __int_as_float(0xff800000) : __int_as_float(0x7f800000);
+    }
+    static __device__ __forceinline__ float op(float a, float b)
+    {
+        return OP == RED_SUM ? __fadd_rn(a, b) : OP == RED_PROD ? __fmul_rn(a, b) : OP == RED_MAX ? fmaxf(a, b) : fminf(a, b);
+    }
+};
+
+template <int OP>
+struct Comb<OP, int32_t> {
+    static __device__ __forceinline__ int32_t identity()
+    {
+        return OP == RED_SUM ? 0 : OP == RED_PROD ? 1 : OP == RED_MAX ? INT32_MIN : INT32_MAX;
+    }
+    static __device__ __forceinline__ int32_t op(int32_t a, int32_t b)
+    {
+        if (OP == RED_SUM)
+            return (int32_t)((uint32_t)a + (uint32_t)b);
+        if (OP == RED_PROD)
+            return (int32_t)((uint32_t)a * (uint32_t)b);
+        return OP == RED_MAX ? (a > b ? a : b) : (a < b ? a : b);
+    }
+};
+
+template <int OP>
+struct Comb<OP, uint32_t> {
+    static __device__ __forceinline__ uint32_t identity()
+    {
+        return OP == RED_SUM ? 0u : OP == RED_PROD ? 1u : OP == RED_MAX ? 0u : 0xffffffffu;
+    }
+    static __device__ __forceinline__ uint32_t op(uint32_t a, uint32_t b)
+    {
+        if (OP == RED_SUM)
+            return a + b;
+        if (OP == RED_PROD)
+            return a * b;
+        return OP == RED_MAX ? (a > b ? a : b) : (a < b ? a : b);
+    }
+};
+
+template <typename A>
+__device__ __forceinline__ A ldcg_a(const A *p);
+template <>
+__device__ __forceinline__ float ldcg_a<float>(const float *p) { return __ldcg(p); }
+template <>
+__device__ __forceinline__ int32_t ldcg_a<int32_t>(const int32_t *p) { return __ldcg(p); }
+template <>
+__device__ __forceinline__ uint32_t ldcg_a<uint32_t>(const uint32_t *p) { return __ldcg(p); }
+
+// V elements of a row starting at element p, widened to A.  V * sizeof(T)
+// is 32 (256-bit load), 16 (128-bit load) or sizeof(T) (one element).
+template <int DT, int V>
+__device__ __forceinline__ void load_row(const typename Elem<DT>::T *p, typename Elem<DT>::A (&v)[V])
+{
+    using E = Elem<DT>;
+    using T = typename E::T;
+    constexpr int BYTES = V * (int)sizeof(T);
+    if constexpr (BYTES == 32 || BYTES == 16) {
+        constexpr int W = BYTES / 4;
+        uint32_t w[W];
+        if constexpr (W == 8) {
+            uint32_t (&w8)[8] = w;
+            ld8u(reinterpret_cast<const uint32_t *>(p), w8);
+        } else {
+            uint32_t (&w4)[4] = w;
+            ld4u(reinterpret_cast<const uint32_t *>(p), w4);
+        }
+        if constexpr (sizeof(T) == 4) {
+#pragma unroll
+            for (int k = 0; k < V; ++k)
+                v[k] = E::widen(w[k]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+                v[2 * k] = E::widen(w[k] & 0xffffu);
+                v[2 * k + 1] = E::widen(w[k] >> 16);
+            }
+        }
+    } else {
+        if constexpr (sizeof(T) == 4)
+            v[0] = E::widen(__ldg(reinterpret_cast<const unsigned int *>(p)));
+        else
+            v[0] = E::widen(__ldg(reinterpret_cast<const unsigned short *>(p)));
+    }
+}
+
+template <int OP, int DT, int V>
+__global__ void __launch_bounds__(CP_NT, 2)
+cols_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t R, int64_t C, int64_t rows_per_split,
+            typename Elem<DT>::A *__restrict__ part, unsigned *__restrict__ tick, typename Elem<DT>::T *__restrict__ out)
+{
+    using E = Elem<DT>;
+    using A = typename E::A;
+    using K = Comb<OP, A>;
+    constexpr int U = sizeof(typename E::T) == 4 ? 4 : 2;  // rows in flight per thread (128 bytes)
+    __shared__ A s_p[CP_WY][32 * V];
+    __shared__ int s_last;
+
+    const int lane = threadIdx.x & 31, wy = threadIdx.x >> 5;
+    const int64_t col = ((int64_t)blockIdx.x * 32 + lane) * V;
+    const bool live = col < C;  // V > 1 only when C % V == 0
+    const int64_t i0 = (int64_t)blockIdx.y * rows_per_split;
+    const int64_t i1 = (i0 + rows_per_split < R) ? i0 + rows_per_split : R;
+
+    A p[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k)
+        p[k] = K::identity();
+    if (live) {
+        const typename E::T *q = x + col;
+        int64_t i = i0 + wy;
+        for (; i + (U - 1) * CP_WY < i1; i += U * CP_WY) {
+            A v[U][V];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                load_row<DT, V>(q + (i + u * CP_WY) * C, v[u]);
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int k = 0; k < V; ++k)
+                    p[k] = K::op(p[k], v[u][k]);
+        }
+        for (; i < i1; i += CP_WY) {
+            A v[V];
+            load_row<DT, V>(q + i * C, v);
+#pragma unroll
+            for (int k = 0; k < V; ++k)
+                p[k] = K::op(p[k], v[k]);
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < V; ++k)
+        s_p[wy][lane * V + k] = p[k];
+    __syncthreads();
+    if (wy == 0) {
+#pragma unroll
+        for (int w = 1; w < CP_WY; ++w)
+#pragma unroll
+            for (int k = 0; k < V; ++k)
+                p[k] = K::op(p[k], s_p[w][lane * V + k]);
+    }
+
+    if (gridDim.y == 1) {
+        if (wy == 0 && live)
+#pragma unroll
+            for (int k = 0; k < V; ++k)
+                out[col + k] = E::narrow(p[k]);
+        return;
+    }
+    if (wy == 0 && live)
+#pragma unroll
+        for (int k = 0; k < V; ++k)
+            part[(int64_t)blockIdx.y * C + col + k] = p[k];
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0)
+        s_last = (atomicAdd(tick + blockIdx.x, 1u) == gridDim.y - 1);
+    __syncthreads();
+    if (!s_last)
+        return;
+    __threadfence();
+    if (wy == 0 && live) {
+        A q[V];
+#pragma unroll
+        for (int k = 0; k < V; ++k)
+            q[k] = K::identity();
+        for (unsigned sp = 0; sp < gridDim.y; ++sp)
+#pragma unroll
+            for (int k = 0; k < V; ++k)
+                q[k] = K::op(q[k], ldcg_a<A>(part + (int64_t)sp * C + col + k));
+#pragma unroll
+        for (int k = 0; k < V; ++k)
+            out[col + k] = E::narrow(q[k]);
+    }
+    if (threadIdx.x == 0)
+        tick[blockIdx.x] = 0;
+}
+
+template <int OP, int DT, int V>
+int launch_cols(const void *xv, int64_t R, int64_t C, void *outv, cudaStream_t s, const DeviceInfo &di)
+{
+    using E = Elem<DT>;
+    using T = typename E::T;
+    using A = typename E::A;
+    static int occ = 0;
+    if (occ == 0)
+        occ = occupancy((const void *)cols_kernel<OP, DT, V>, CP_NT);
+    if (occ <= 0)
+        return fail(RED_ECUDA, "red_cols: kernel cannot be resident on this device");
+    constexpr int U = sizeof(T) == 4 ? 4 : 2;
+    const int64_t tile_cols = 32 * V;
+    const int64_t tiles = (C + tile_cols - 1) / tile_cols;
+    if (tiles > 0x7fffffffLL)
+        return fail(RED_EINVAL, "red_cols: C too large");
+    // Row splits: each warp keeps at least U rows; among those counts take
+    // the smallest whose CTAs fill their waves of resident CTAs to at least
+    // 90% (more splits add partial traffic and per-CTA overhead), else the
+    // count with the best wave efficiency.
+    int64_t splits = knob(RED_KNOB_COLPROD_SPLITS);
+    if (splits <= 0) {
+        const int64_t slots = (int64_t)di.sms * occ;
+        int64_t smax = R / (CP_WY * U);
+        if (smax > 4096)
+            smax = 4096;
+        if (smax < 1)
+            smax = 1;
+        splits = 1;
+        double best = -1.0;
+        for (int64_t sp = 1; sp <= smax; ++sp) {
+            const int64_t ctas = tiles * sp;
+            const double eff = (double)ctas / (double)(((ctas + slots - 1) / slots) * slots);
+            if (eff >= 0.9) {
+                splits = sp;
+                break;
+            }
+            if (eff > best) {
+                best = eff;
+                splits = sp;
+            }
+        }
+    }
+    if (splits > R)
+        splits = R;
+    if (splits > 65535)
+        splits = 65535;
+    if (splits * C > (int64_t)WS_PART_ELEMS)
+        splits = (int64_t)WS_PART_ELEMS / C;
+    if (tiles > WS_TICKETS)
+        splits = 1;
+    if (splits < 1)
+        splits = 1;
+    const int64_t rps = (R + splits - 1) / splits;
+    splits = (R + rps - 1) / rps;  // no empty split
+    Workspace ws;
+    if (splits > 1) {
+        const int st = get_workspace(&ws);
+        if (st != RED_OK)
+            return st;
+    }
+    const dim3 grid((unsigned)tiles, (unsigned)splits);
+    cols_kernel<OP, DT, V><<<grid, CP_NT, 0, s>>>(static_cast<const T *>(xv), R, C, rps, static_cast<A *>(ws.part),
+                                                  ws.tick, static_cast<T *>(outv));
+    count_launches(1);
+    return cuda_fail(cudaGetLastError(), "red_cols launch");
+}
+
+// Vector width by alignment: 32-byte rows and base -> 256-bit loads,
+// 16-byte -> 128-bit, otherwise one element per lane.
+template <int OP, int DT>
+int launch_cols_dt(const void *x, int64_t R, int64_t C, void *out, cudaStream_t s, const DeviceInfo &di)
+{
+    constexpr int SZ = (int)sizeof(typename Elem<DT>::T);
+    const uintptr_t a = (uintptr_t)x;
+    const int64_t row_bytes = C * SZ;
+    if (row_bytes % 32 == 0 && a % 32 == 0)
+        return launch_cols<OP, DT, 32 / SZ>(x, R, C, out, s, di);
+    if (row_bytes % 16 == 0 && a % 16 == 0)
+        return launch_cols<OP, DT, 16 / SZ>(x, R, C, out, s, di);
+    return launch_cols<OP, DT, 1>(x, R, C, out, s, di);
+}
+
+template <int OP>
+int launch_cols_op(int dtype, const void *x, int64_t R, int64_t C, void *out, cudaStream_t s, const DeviceInfo &di)
+{
+    switch (dtype) {
+    case RED_F32: return launch_cols_dt<OP, RED_F32>(x, R, C, out, s, di);
+    case RED_I32: return launch_cols_dt<OP, RED_I32>(x, R, C, out, s, di);
+    case RED_F16: return launch_cols_dt<OP, RED_F16>(x, R, C, out, s, di);
+    case RED_BF16: return launch_cols_dt<OP, RED_BF16>(x, R, C, out, s, di);
+    case RED_I16: return launch_cols_dt<OP, RED_I16>(x, R, C, out, s, di);
+    case RED_U16: return launch_cols_dt<OP, RED_U16>(x, R, C, out, s, di);
+    default: return launch_cols_dt<OP, RED_U32>(x, R, C, out, s, di);
+    }
+}
+
+}  // namespace
+
+int launch_cols(int op, int dtype, const void *x, int64_t R, int64_t C, void *out, cudaStream_t s)
+{
+    DeviceInfo di;
+    const int st = device_info(&di);
+    if (st != RED_OK)
+        return st;
+    switch (op) {
+    case RED_SUM: return launch_cols_op<RED_SUM>(dtype, x, R, C, out, s, di);
+    case RED_MAX: return launch_cols_op<RED_MAX>(dtype, x, R, C, out, s, di);
+    case RED_MIN: return launch_cols_op<RED_MIN>(dtype, x, R, C, out, s, di);
+    default: return launch_cols_op<RED_PROD>(dtype, x, R, C, out, s, di);
+    }
+}
+
+}  // namespace red

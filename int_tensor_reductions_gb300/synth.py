@@ -126,3 +126,31 @@ def cfg5(device="cpu", rows: int = CFG5_ROWS, minlen: int = CFG5_MINLEN, maxlen:
     nnz = int(off[-1].item())
     x = ragged_values(nnz, -4.0, 4.0, 5, device)
     return x, off
+
+
+# ------------------------------------------- column reductions, all types
+
+COL_STORAGE = {"f32": torch.float32, "i32": torch.int32, "u32": torch.int32, "f16": torch.float16,
+               "bf16": torch.bfloat16, "i16": torch.int16, "u16": torch.int16}
+
+
+def col_input(op: str, dtype: str, shape, seed: int, device="cpu") -> torch.Tensor:
+    """Seeded input for a column reduction of element type ``dtype`` ("f32",
+    "i32", "u32", "f16", "bf16", "i16", "u16"); u16 / u32 come back in
+    int16 / int32 storage holding the unsigned bit patterns.  Products get
+    values that keep long products finite: uniform[0.99, 1.01] for floating
+    types, {+-1, +-2, +-3} (unsigned: {1, 2, 3}) for integers; the other
+    operators get uniform[-1, 1) floats or integers over the type's range."""
+    g = _gen(seed, device)
+    if dtype in ("f32", "f16", "bf16"):
+        lo, hi = (0.99, 1.01) if op == "prod" else (-1.0, 1.0)
+        x = torch.rand(shape, generator=g, device=device, dtype=torch.float32).mul_(hi - lo).add_(lo)
+        return _post(x).to(COL_STORAGE[dtype])
+    if op == "prod":
+        choices = (1, 2, 3) if dtype in ("u16", "u32") else INT_CHOICES
+        idx = torch.randint(0, len(choices), shape, generator=g, device=device)
+        return torch.tensor(choices, dtype=torch.int64, device=device)[idx].to(COL_STORAGE[dtype])
+    bits = 16 if dtype in ("i16", "u16") else 32
+    # the type's full bit range, drawn in int64 and stored two's complement
+    v = torch.randint(-(1 << (bits - 1)), 1 << (bits - 1), shape, generator=g, device=device, dtype=torch.int64)
+    return v.to(COL_STORAGE[dtype])

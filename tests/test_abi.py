@@ -72,7 +72,12 @@ def test_rows_reject_bad_arguments(lib):
 
 def test_colprod_rejects_and_returns_early(lib):
     from int_tensor_reductions_gb300 import RED_EINVAL, RED_F32, RED_OK
-    assert lib.red_colprod(5, 0x1000, 4, 4, 0x2000, None) == RED_EINVAL
+    assert lib.red_colprod(9, 0x1000, 4, 4, 0x2000, None) == RED_EINVAL
+    assert lib.red_cols(4, RED_F32, 0x1000, 4, 4, 0x2000, None) == RED_EINVAL   # unknown op
+    assert lib.red_cols(3, 7, 0x1000, 4, 4, 0x2000, None) == RED_EINVAL         # unknown dtype
+    assert lib.red_cols(0, RED_F32, 0x1002, 4, 4, 0x2000, None) == RED_EINVAL   # f32 at 2-byte offset
+    assert lib.red_cols(0, 2, 0x1001, 4, 4, 0x2000, None) == RED_EINVAL         # f16 at odd address
+    assert lib.red_cols(1, 4, None, 0, 4, None, None) == RED_OK                 # early return
     assert lib.red_colprod(RED_F32, 0x1000, -1, 4, 0x2000, None) == RED_EINVAL
     # pto-isa docs, "TCOLPROD", "Constraints": empty tile -> early return
     assert lib.red_colprod(RED_F32, None, 0, 4, None, None) == RED_OK

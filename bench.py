@@ -434,6 +434,7 @@ def run_ours(args):
     if not args.no_supplementary:
         result["fused_stats_2p30"] = fused_stats(w, stream, per_op)
         result["supplementary_1gib"] = supplementary(stream, dev, peak)
+        result["column_ops"] = column_ops(stream, dev, peak)
 
     if not args.no_e2e:
         result["e2e"] = run_e2e(w, calls, stream, args.e2e_steps, world, dist, dev)
@@ -538,6 +539,36 @@ def supplementary(stream, dev, peak, reps=10):
     del x, o
     torch.cuda.empty_cache()
     return out
+
+
+def column_ops(stream, dev, peak, reps=10):
+    """Column reductions of the other element types and operators (TCOLPROD's
+    siblings), each on an input larger than L2: GB/s of algorithmic bytes."""
+    import torch
+    import int_tensor_reductions_gb300 as itr
+    from int_tensor_reductions_gb300 import synth
+    res = {"unit": "GB/s", "note": "back-to-back calls, inputs > L2 except the 8 MiB int16 case"}
+    for op, dtype, R, C in (("sum", "f32", 4096, 16384), ("prod", "f16", 4096, 16384), ("sum", "bf16", 8192, 16384),
+                            ("max", "u32", 4096, 16384), ("prod", "i16", 64, 65536)):
+        x = synth.col_input(op, dtype, (R, C), 11, dev)
+        o = torch.empty(C, dtype=x.dtype, device=dev)
+        for _ in range(2):
+            itr.red_cols(op, x, o, dtype=dtype)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            itr.red_cols(op, x, o, dtype=dtype)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        nbytes = x.numel() * x.element_size() + C * x.element_size()
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[f"{op} {dtype} {R}x{C}"] = {"us": round(ms * 1e3, 1), "gbs": round(gbs, 1),
+                                       "frac_of_peak": round(gbs / peak, 4)}
+        del x, o
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_e2e(w, calls, stream, steps, world, dist, dev):

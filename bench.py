@@ -435,6 +435,7 @@ def run_ours(args):
         result["fused_stats_2p30"] = fused_stats(w, stream, per_op)
         result["supplementary_1gib"] = supplementary(stream, dev, peak)
         result["column_ops"] = column_ops(stream, dev, peak)
+        result["typed_ops"] = typed_ops(stream, dev, peak)
 
     if not args.no_e2e:
         result["e2e"] = run_e2e(w, calls, stream, args.e2e_steps, world, dist, dev)
@@ -566,6 +567,42 @@ def column_ops(stream, dev, peak, reps=10):
         gbs = nbytes / (ms * 1e-3) / 1e9
         res[f"{op} {dtype} {R}x{C}"] = {"us": round(ms * 1e3, 1), "gbs": round(gbs, 1),
                                        "frac_of_peak": round(gbs / peak, 4)}
+        del x, o
+    torch.cuda.empty_cache()
+    return res
+
+
+def typed_ops(stream, dev, peak, reps=10):
+    """Full and row reductions of other element types (red_full_typed,
+    red_rows_typed) on inputs larger than L2: GB/s of algorithmic bytes."""
+    import torch
+    import int_tensor_reductions_gb300 as itr
+    from int_tensor_reductions_gb300 import synth
+    res = {"unit": "GB/s", "note": "back-to-back calls, inputs > L2"}
+    cases = (("full", "sum", "i32", (1 << 28,)), ("full", "max", "f16", (1 << 29,)),
+             ("rows", "sum", "i32", (65536, 1024)), ("rows", "max", "bf16", (65536, 2048)))
+    for kind, op, dtype, shape in cases:
+        x = synth.col_input(op, dtype, shape, 12, dev)
+        if kind == "full":
+            o = torch.empty(1, dtype=x.dtype, device=dev)
+            fn = lambda: itr.red_full_typed(op, x, o, dtype=dtype)  # noqa: E731
+        else:
+            o = torch.empty(shape[0], dtype=x.dtype, device=dev)
+            fn = lambda: itr.red_rows_typed(op, x, out=o, dtype=dtype)  # noqa: E731
+        for _ in range(2):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / reps
+        nbytes = (x.numel() + o.numel()) * x.element_size()
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[f"{kind} {op} {dtype} {'x'.join(map(str, shape))}"] = {"us": round(ms * 1e3, 1), "gbs": round(gbs, 1),
+                                                                   "frac_of_peak": round(gbs / peak, 4)}
         del x, o
     torch.cuda.empty_cache()
     return res

@@ -201,6 +201,24 @@ int red_rows_ragged(int op, const float *x, const int64_t *offsets, int64_t rows
 int red_cols(int op, int dtype, const void *x, int64_t R, int64_t C, void *out, red_stream_t stream);
 
 /*
+ * red_full_typed / red_rows_typed -- red_full and red_rows for every element
+ * type of red_cols (enum red_dtype) and every operator including RED_PROD:
+ * out[0] = op over x[0..n); out[r] = op over row r = x[r*len .. r*len+len),
+ * with accum != 0 folding the old out[r] in as one more operand ([TVM] "How
+ * inputs change the algorithm").  Arithmetic as red_cols: floating types
+ * accumulate in fp32 and round once to the element type, integer sums and
+ * products wrap modulo 2^bits, max / min compare values.  x and out hold the
+ * element type and are aligned to its size.
+ *   Empty input: RED_SUM writes 0 and RED_PROD writes 1 (with accum, rows are
+ *   left unchanged); RED_MAX / RED_MIN return RED_EINVAL.
+ * The fp32 fast paths (packed folds, 256-bit loads) are red_full / red_rows;
+ * these are the general-type versions.
+ */
+int red_full_typed(int op, int dtype, const void *x, int64_t n, void *out, red_stream_t stream);
+int red_rows_typed(int op, int dtype, const void *x, int64_t rows, int64_t len, int accum, void *out,
+                   red_stream_t stream);
+
+/*
  * red_colprod -- [PTO] TCOLPROD: red_cols(RED_PROD, dtype, ...).
  *   dtype  any enum red_dtype; RED_F32 products round to nearest in fp32,
  *          RED_I32 (and the other integer types) wrap modulo 2^bits.

@@ -11,6 +11,7 @@ libred.so is missing or CUDA is unavailable, the calls raise.
     red_rows_ragged(op, x, offsets, accum=False, out=None)
     red_colprod(x, out=None)                       x: (R, C) of any column element type
     red_cols(op, x, out=None)                      column sum / max / min / prod
+    red_full_typed / red_rows_typed                 full / per-row ops for every element type
     red_full_stats(x, out=None)                    sum, max, min, sum|x| in one read
     red_rows_thread(op, x, accum=False, out=None)  one thread per row, the page's fold order
 """
@@ -18,6 +19,6 @@ from ._binding import (  # noqa: F401
     RED_BF16, RED_EINVAL, RED_ECUDA, RED_ENOMEM, RED_F16, RED_F32, RED_I16, RED_I32, RED_KNOB_COLPROD_SPLITS,
     RED_KNOB_FULL_CTAS_PER_SM, RED_KNOB_RAGGED_GROUP, RED_KNOB_ROWS_GROUP, RED_MAX, RED_MIN,
     RED_MODE_ATOMIC, RED_MODE_AUTO, RED_MODE_LAST_BLOCK, RED_MODE_TWO_PASS, RED_OK, RED_PROD, RED_SUM, RED_U16, RED_U32,
-    RedError, lib, lib_path, red_colprod, red_cols, red_full, red_full_noalloc, red_full_stats, red_get_full_mode, red_get_knob, red_last_error, red_launch_count,
-    red_release_workspace, red_rows, red_rows_ragged, red_rows_thread, red_set_full_mode, red_set_knob, red_version,
+    RedError, lib, lib_path, red_colprod, red_cols, red_full, red_full_noalloc, red_full_stats, red_full_typed, red_get_full_mode, red_get_knob, red_last_error, red_launch_count,
+    red_release_workspace, red_rows, red_rows_ragged, red_rows_thread, red_rows_typed, red_set_full_mode, red_set_knob, red_version,
 )

@@ -35,6 +35,8 @@ _SIGNATURES = {
     "red_rows_thread": ([_int, _vp, _i64, _int, _int, _vp, _vp], _int),
     "red_colprod": ([_int, _vp, _i64, _i64, _vp, _vp], _int),
     "red_cols": ([_int, _int, _vp, _i64, _i64, _vp, _vp], _int),
+    "red_full_typed": ([_int, _int, _vp, _i64, _vp, _vp], _int),
+    "red_rows_typed": ([_int, _int, _vp, _i64, _i64, _int, _vp, _vp], _int),
     "red_set_full_mode": ([_int], _int),
     "red_get_full_mode": ([], _int),
     "red_set_knob": ([_int, _int], _int),
@@ -233,6 +235,46 @@ def red_cols(op, x: torch.Tensor, out: torch.Tensor | None = None, stream=None, 
         raise ValueError("out must have C elements")
     with torch.cuda.device(x.device):
         _check(lib().red_cols(_op(op), code, x.data_ptr(), R, C, out.data_ptr(), _stream(stream, x.device)))
+    return out
+
+
+def red_full_typed(op, x: torch.Tensor, out: torch.Tensor | None = None, stream=None, dtype=None) -> torch.Tensor:
+    """op ("sum", "max", "min", "prod") over all of x, for every element type
+    red_cols accepts; ``out`` (shape (1,)) has x's element type."""
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor")
+    code = _col_dtype(x, dtype)
+    if out is None:
+        out = torch.empty(1, dtype=x.dtype, device=x.device)
+    if not out.is_cuda or out.element_size() != x.element_size():
+        raise ValueError("out must be a CUDA tensor of x's element size")
+    with torch.cuda.device(x.device):
+        _check(lib().red_full_typed(_op(op), code, x.data_ptr(), x.numel(), out.data_ptr(),
+                                    _stream(stream, x.device)))
+    return out
+
+
+def red_rows_typed(op, x: torch.Tensor, accum: bool = False, out: torch.Tensor | None = None, stream=None,
+                   dtype=None) -> torch.Tensor:
+    """Per-row op of a (rows, len) matrix of any element type red_cols accepts,
+    optionally folding the old out[r] in (accum)."""
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor")
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D (rows, len)")
+    code = _col_dtype(x, dtype)
+    rows, length = x.shape
+    if out is None:
+        if accum:
+            raise ValueError("accum needs an existing out")
+        out = torch.empty(rows, dtype=x.dtype, device=x.device)
+    if not out.is_cuda or not out.is_contiguous() or out.element_size() != x.element_size():
+        raise ValueError("out must be a contiguous CUDA tensor of x's element size")
+    if out.numel() != rows:
+        raise ValueError("out must have one element per row")
+    with torch.cuda.device(x.device):
+        _check(lib().red_rows_typed(_op(op), code, x.data_ptr(), rows, length, int(bool(accum)), out.data_ptr(),
+                                    _stream(stream, x.device)))
     return out
 
 

@@ -245,6 +245,48 @@ int red_cols(int op, int dtype, const void *x, int64_t R, int64_t C, void *out, 
     return launch_cols(op, dtype, x, R, C, out, reinterpret_cast<cudaStream_t>(stream));
 }
 
+namespace {
+uintptr_t elem_bytes(int dtype) { return (dtype == RED_F32 || dtype == RED_I32 || dtype == RED_U32) ? 4 : 2; }
+}  // namespace
+
+int red_full_typed(int op, int dtype, const void *x, int64_t n, void *out, red_stream_t stream)
+{
+    if (op < RED_SUM || op > RED_PROD)
+        return fail(RED_EINVAL, "red_full_typed: unknown op %d", op);
+    if (dtype < RED_F32 || dtype > RED_U32)
+        return fail(RED_EINVAL, "red_full_typed: unknown dtype %d", dtype);
+    if (n < 0 || n > MAX_ELEMS)
+        return fail(RED_EINVAL, "red_full_typed: n = %lld out of range", (long long)n);
+    if (n == 0 && (op == RED_MAX || op == RED_MIN))
+        return fail(RED_EINVAL, "red_full_typed: max/min of an empty vector");
+    if (!out || misaligned(out, elem_bytes(dtype)))
+        return fail(RED_EINVAL, "red_full_typed: out is NULL or not aligned to its element size");
+    if (n > 0 && (!x || misaligned(x, elem_bytes(dtype))))
+        return fail(RED_EINVAL, "red_full_typed: x is NULL or not aligned to its element size");
+    return launch_typed(true, op, dtype, x, 1, n, 0, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int red_rows_typed(int op, int dtype, const void *x, int64_t rows, int64_t len, int accum, void *out,
+                   red_stream_t stream)
+{
+    if (op < RED_SUM || op > RED_PROD)
+        return fail(RED_EINVAL, "red_rows_typed: unknown op %d", op);
+    if (dtype < RED_F32 || dtype > RED_U32)
+        return fail(RED_EINVAL, "red_rows_typed: unknown dtype %d", dtype);
+    if (rows < 0 || len < 0 || rows > MAX_ELEMS || len > MAX_ELEMS || (len > 0 && rows > MAX_ELEMS / len))
+        return fail(RED_EINVAL, "red_rows_typed: rows = %lld, len = %lld out of range", (long long)rows,
+                    (long long)len);
+    if (rows == 0)
+        return RED_OK;
+    if (len == 0 && (op == RED_MAX || op == RED_MIN))
+        return fail(RED_EINVAL, "red_rows_typed: max/min of empty rows");
+    if (!out || misaligned(out, elem_bytes(dtype)))
+        return fail(RED_EINVAL, "red_rows_typed: out is NULL or not aligned to its element size");
+    if (len > 0 && (!x || misaligned(x, elem_bytes(dtype))))
+        return fail(RED_EINVAL, "red_rows_typed: x is NULL or not aligned to its element size");
+    return launch_typed(false, op, dtype, x, rows, len, accum ? 1 : 0, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int red_colprod(int dtype, const void *x, int64_t R, int64_t C, void *out, red_stream_t stream)
 {
     if (dtype < RED_F32 || dtype > RED_U32)

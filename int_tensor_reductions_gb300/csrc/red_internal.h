@@ -51,6 +51,8 @@ int launch_rows(int op, const float *x, int64_t rows, int64_t len, int accum, fl
                 cudaStream_t s);
 int launch_ragged(int op, const float *x, const int64_t *off, int64_t rows, int64_t nnz, int accum,
                   float *out, cudaStream_t s);
+int launch_typed(bool full, int op, int dtype, const void *x, int64_t rows, int64_t len, int accum, void *out,
+                 cudaStream_t s);
 int launch_cols(int op, int dtype, const void *x, int64_t R, int64_t C, void *out, cudaStream_t s);
 
 // Resident CTAs per SM of a kernel at `threads` threads and no dynamic shared

@@ -67,6 +67,8 @@ def _load():
     lib.orc_bf16_to_double.restype = ctypes.c_double
     sigs["orc_cols_f"] = [i32, i32, vp, i64, i64, vp, vp]
     sigs["orc_cols_i"] = [i32, i32, vp, i64, i64, vp]
+    sigs["orc_rows_typed_f"] = [i32, i32, vp, i64, i64, i32, vp, vp, vp]
+    sigs["orc_rows_typed_i"] = [i32, i32, vp, i64, i64, i32, vp, vp]
     for name, args in sigs.items():
         fn = getattr(lib, name)
         fn.argtypes = args
@@ -249,3 +251,24 @@ def cols(op, dtype, x, R, C, out=None):
     res = np.zeros(C, np.int64) if out is None else out
     _check(lib.orc_cols_i(COL_OPS[op], COL_DTYPES[dtype], _ptr(raw), R, C, _ptr(res)), "cols_i")
     return res
+
+
+def rows_typed(op, dtype, x, rows_, len_, accum=False, dst_old=None):
+    """Per-row op of a row-major rows_ x len_ matrix in raw element storage
+    (a full vector is rows_ = 1).  Floating types return (float64[rows]
+    result, float64[rows] sum|x|); integer types int64[rows]."""
+    raw = np.ascontiguousarray(x).view(np.uint8).reshape(-1)
+    if raw.size != rows_ * len_ * _COL_BYTES[dtype]:
+        raise OracleError("x has the wrong size")
+    d = None if not accum else np.ascontiguousarray(dst_old).view(np.uint8).reshape(-1)
+    lib = _load()
+    if dtype in ("f32", "f16", "bf16"):
+        out = np.zeros(rows_, np.float64)
+        ab = np.zeros(rows_, np.float64)
+        _check(lib.orc_rows_typed_f(COL_OPS[op], COL_DTYPES[dtype], _ptr(raw), rows_, len_, int(bool(accum)),
+                                    _ptr(d), _ptr(out), _ptr(ab)), "rows_typed_f")
+        return out, ab
+    out = np.zeros(rows_, np.int64)
+    _check(lib.orc_rows_typed_i(COL_OPS[op], COL_DTYPES[dtype], _ptr(raw), rows_, len_, int(bool(accum)),
+                                _ptr(d), _ptr(out)), "rows_typed_i")
+    return out

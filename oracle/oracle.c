@@ -469,3 +469,94 @@ int orc_cols_i(int op, int dtype, const void *x, int64_t R, int64_t C, int64_t *
     }
     return ORC_OK;
 }
+
+/* ----------------------------------------- typed full and row reductions --- */
+
+/* Row r = x[r*len .. r*len+len) of a floating element type; out[r] = op over
+ * the row in double, started from the old dst value when accum ([TVM] "How
+ * inputs change the algorithm": the old value is one more operand);
+ * abs_out[r] = sum of |row| (+ |old|).  An empty row gives 0 for sum, 1 for
+ * product (the old value with accum); empty max / min rows are rejected.  A
+ * full vector is the case rows = 1. */
+int orc_rows_typed_f(int op, int dtype, const void *x, int64_t rows, int64_t len, int accum,
+                     const void *dst_old, double *out, double *abs_out)
+{
+    if (op < ORC_SUM || op > ORC_PROD || !(dtype == ORC_F32 || dtype == ORC_F16 || dtype == ORC_BF16) ||
+        rows < 0 || len < 0 || (rows > 0 && (!out || !abs_out)) || (rows > 0 && len > 0 && !x) ||
+        (accum && rows > 0 && !dst_old) || (rows > 0 && len == 0 && (op == ORC_MAX || op == ORC_MIN) && !accum))
+        return ORC_EINVAL;
+    for (int64_t r = 0; r < rows; ++r) {
+        double acc, a = 0.0;
+        int64_t k = 0;
+        if (accum) {
+            acc = elem_f(dst_old, dtype, r);
+            a = fabs(acc);
+        } else if (len > 0) {
+            acc = elem_f(x, dtype, r * len);
+            a = fabs(acc);
+            k = 1;
+        } else {
+            acc = op == ORC_PROD ? 1.0 : 0.0;
+        }
+        for (; k < len; ++k) {
+            const double v = elem_f(x, dtype, r * len + k);
+            a += fabs(v);
+            if (op == ORC_SUM)
+                acc += v;
+            else if (op == ORC_PROD)
+                acc *= v;
+            else if (op == ORC_MAX)
+                acc = v > acc ? v : acc;
+            else
+                acc = v < acc ? v : acc;
+        }
+        out[r] = acc;
+        abs_out[r] = a;
+    }
+    return ORC_OK;
+}
+
+/* The same for an integer element type: sums and products wrap modulo
+ * 2^bits of the type; out[r] is the result as a sign-extended int64. */
+int orc_rows_typed_i(int op, int dtype, const void *x, int64_t rows, int64_t len, int accum,
+                     const void *dst_old, int64_t *out)
+{
+    if (op < ORC_SUM || op > ORC_PROD ||
+        !(dtype == ORC_I32 || dtype == ORC_U32 || dtype == ORC_I16 || dtype == ORC_U16) || rows < 0 ||
+        len < 0 || (rows > 0 && !out) || (rows > 0 && len > 0 && !x) || (accum && rows > 0 && !dst_old) ||
+        (rows > 0 && len == 0 && (op == ORC_MAX || op == ORC_MIN) && !accum))
+        return ORC_EINVAL;
+    const int bits = 8 * elem_size(dtype);
+    const uint64_t mask = (1ull << bits) - 1;
+    const int is_signed = dtype == ORC_I32 || dtype == ORC_I16;
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t m;
+        int64_t k = 0;
+        if (accum) {
+            m = elem_i(dst_old, dtype, r);
+        } else if (len > 0) {
+            m = elem_i(x, dtype, r * len);
+            k = 1;
+        } else {
+            m = op == ORC_PROD ? 1 : 0;
+        }
+        uint64_t w = (uint64_t)m;
+        for (; k < len; ++k) {
+            const int64_t v = elem_i(x, dtype, r * len + k);
+            if (op == ORC_SUM)
+                w += (uint64_t)v;
+            else if (op == ORC_PROD)
+                w *= (uint64_t)v;
+            else if (op == ORC_MAX)
+                m = v > m ? v : m;
+            else
+                m = v < m ? v : m;
+        }
+        if (op == ORC_SUM || op == ORC_PROD) {
+            w &= mask;
+            m = (is_signed && (w >> (bits - 1)) & 1u) ? (int64_t)w - (int64_t)(mask + 1) : (int64_t)w;
+        }
+        out[r] = m;
+    }
+    return ORC_OK;
+}

@@ -24,6 +24,7 @@ DTYPES = ["f32", "i32", "u32", "f16", "bf16", "i16", "u16"]
 OPS = ["sum", "max", "min", "prod"]
 NP_INT = {"i32": np.int32, "u32": np.uint32, "i16": np.int16, "u16": np.uint16}
 MANT = {"f16": 10, "bf16": 7}
+EMIN = {10: -14, 7: -126}  # smallest normal exponent of half / bfloat16
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -46,7 +47,9 @@ def _decode(t: torch.Tensor, dtype: str) -> np.ndarray:
 
 def _ulp(v, mant):
     a = np.abs(v)
-    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    # spacing of the type at |v|, floored at its subnormal spacing (a result
+    # below the type's range rounds to a subnormal or zero)
+    e = np.maximum(np.floor(np.log2(np.where(a > 0, a, 1.0))), EMIN[mant])
     return np.exp2(e - mant)
 
 

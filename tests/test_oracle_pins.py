@@ -458,3 +458,38 @@ def test_cols_f32_product_matches_colprod():
     got, _ = oracle.cols("prod", "f32", x, 30, 7)
     _, pd = oracle.colprod_f32(x, 30, 7, want_double=True)
     assert (got == pd).all()
+
+
+# ------------------------------------------------ typed rows (all element types)
+
+def test_rows_typed_agree_with_columns_of_the_transpose():
+    """Row r of x is column r of x^T: the typed row oracle and the column
+    oracle (pinned above) must agree on every type and operator."""
+    rng = np.random.default_rng(8)
+    for dtype, npt in [("i32", np.int32), ("u32", np.uint32), ("i16", np.int16), ("u16", np.uint16)]:
+        info = np.iinfo(npt)
+        x = rng.integers(int(info.min), int(info.max) + 1, size=(6, 11), dtype=np.int64).astype(npt)
+        for op in ("sum", "prod", "max", "min"):
+            assert (oracle.rows_typed(op, dtype, x, 6, 11) ==
+                    oracle.cols(op, dtype, np.ascontiguousarray(x.T), 11, 6)).all(), (dtype, op)
+    x = rng.uniform(0.5, 1.5, size=(5, 9)).astype(np.float16)
+    for op in ("sum", "prod", "max", "min"):
+        a, _ = oracle.rows_typed(op, "f16", x, 5, 9)
+        b, _ = oracle.cols(op, "f16", np.ascontiguousarray(x.T), 9, 5)
+        assert (a == b).all(), op
+
+
+def test_rows_typed_accum_and_empty():
+    x = np.array([[2, 3], [4, 5]], np.int16)
+    old = np.array([10, -1], np.int16)
+    assert oracle.rows_typed("sum", "i16", x, 2, 2, True, old).tolist() == [15, 8]
+    assert oracle.rows_typed("prod", "i16", x, 2, 2, True, old).tolist() == [60, -20]
+    assert oracle.rows_typed("max", "i16", x, 2, 2, True, old).tolist() == [10, 5]
+    e = np.zeros((3, 0), np.int32)
+    assert oracle.rows_typed("prod", "i32", e, 3, 0).tolist() == [1, 1, 1]
+    assert oracle.rows_typed("sum", "i32", e, 3, 0).tolist() == [0, 0, 0]
+    with pytest.raises(oracle.OracleError):
+        oracle.rows_typed("max", "i32", e, 3, 0)
+    r, _ = oracle.rows_typed("sum", "f16", np.full((1, 4), 0.5, np.float16), 1, 4, True,
+                             np.array([1.0], np.float16))
+    assert r.tolist() == [3.0]

@@ -609,19 +609,41 @@ def typed_ops(stream, dev, peak, reps=10):
 
 
 def run_e2e(w, calls, stream, steps, world, dist, dev):
-    """Same step through the public API from pinned host buffers: every step
-    copies its inputs host->device and its results device->host."""
+    """The same step through the public API from pinned host buffers: every
+    step copies its inputs host->device and its results device->host.
+
+    The copies run on a second stream, largest input (the 4 GiB vector) first,
+    and each workload's ops start as soon as its own inputs have landed, so
+    the reductions overlap the remaining copies (the host link, not the
+    GPU, bounds this figure: ~211 GB/s host->device on this machine)."""
     import torch
     host_in = [t.cpu().pin_memory() for t in w.inputs]
     host_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in w.outputs]
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = sum(t.numel() * t.element_size() for t in host_out)
+    copy_stream = torch.cuda.Stream(device=dev)
+    # inputs each op family reads (indices into w.inputs)
+    needs = {"full1": [0], "rows2": [1, 2], "full3": [3], "colprod4a": [4], "colprod4b": [5], "ragged5": [6, 7]}
+    order = [3, 1, 2, 4, 6, 7, 0, 5]  # the 4 GiB vector first
+    fam_order = ["full3", "rows2", "colprod4a", "ragged5", "full1", "colprod4b"]
 
     def step():
-        for d, h in zip(w.inputs, host_in):
-            d.copy_(h, non_blocking=True)
-        for _, _, fn in calls:
-            fn()
+        start = torch.cuda.Event()
+        start.record(stream)
+        copy_stream.wait_event(start)
+        landed = {}
+        with torch.cuda.stream(copy_stream):
+            for i in order:
+                w.inputs[i].copy_(host_in[i], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(copy_stream)
+                landed[i] = ev
+        for fam in fam_order:
+            for i in needs[fam]:
+                stream.wait_event(landed[i])
+            for name, _, fn in calls:
+                if name.split(" ")[0] == fam:
+                    fn()
         for h, d in zip(host_out, w.outputs):
             h.copy_(d, non_blocking=True)
 
@@ -639,7 +661,8 @@ def run_e2e(w, calls, stream, steps, world, dist, dev):
     ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     value = job_gbs(world, w.step_bytes, steps, ms)
     return {"value": round(value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": steps, "ms_per_step": round(ms / steps, 3)}
+            "steps": steps, "ms_per_step": round(ms / steps, 3),
+            "h2d_gbs_seen": round(h2d / (ms / steps * 1e-3) / 1e9, 1)}
 
 
 def cpu_baseline(w):

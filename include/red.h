@@ -40,7 +40,10 @@
  *   - Workspace: partial results of the multi-CTA stages live in a workspace
  *     that the library allocates once per device (16 MiB of partials plus
  *     65536 counters, zeroed at allocation), on the first call that needs it.
- *     That first call should therefore come before any CUDA stream capture.
+ *     That first call should therefore come before any CUDA stream capture;
+ *     after it, the calls of this header other than red_full_noalloc can be
+ *     captured into a CUDA graph and replayed (they then allocate nothing and
+ *     synchronise nothing).
  *     The counters reset themselves at the end of every call, so calls on one
  *     device must be ordered (one stream, or streams ordered by events):
  *     two such calls running at the same time on one device race.

@@ -5,12 +5,15 @@
 // one more operand).  Arithmetic as red_types.cuh states: a 32-bit
 // accumulator per type, one narrowing at the end.
 //
-// Rows: a group of G lanes owns a row; lane l folds elements l, l+G, ... of
-// it (consecutive lanes read consecutive elements), 4 loads in flight; the
-// group combines through a butterfly.  Full vector: every thread of the grid
-// folds elements tid, tid+nthreads, ..., the CTA combines through a warp
-// butterfly and shared memory, and the last CTA to finish folds the CTA
-// partials (last-block grid stage, workspace partials).
+// Both read the span (a row, or the whole vector) as its 32-byte aligned
+// interior in 256-bit blocks (8 or 16 elements each, widened), 4 blocks in
+// flight per thread, plus its unaligned head and tail as naturally aligned
+// pieces of 1, 2, 4 and 8 elements, so every load lies inside the span.
+// Rows: a group of G lanes owns a row and splits its blocks; the group
+// combines through a butterfly.  Full vector: the grid splits the blocks, the
+// CTA combines through a warp butterfly and shared memory, and the last CTA
+// to finish folds the CTA partials (last-block grid stage, workspace
+// partials).
 #include "red_internal.h"
 #include "red_prims.cuh"
 #include "red_types.cuh"
@@ -37,6 +40,126 @@ __device__ __forceinline__ A tree(A v)
     return v;
 }
 
+// Elements per 32-byte block.
+template <int DT>
+__host__ __device__ constexpr int epb() { return 32 / (int)sizeof(typename Elem<DT>::T); }
+
+// Fold the K naturally aligned elements at p (K * element size = 2, 4, 8, 16
+// or 32 bytes) into acc, widened.
+template <int OP, int DT, int K>
+__device__ __forceinline__ void fold_piece(const typename Elem<DT>::T *p, typename Elem<DT>::A &acc)
+{
+    using E = Elem<DT>;
+    using K_ = Comb<OP, typename E::A>;
+    constexpr int SZ = (int)sizeof(typename E::T);
+    constexpr int BYTES = K * SZ;
+    static_assert(BYTES == 2 || BYTES == 4 || BYTES == 8 || BYTES == 16 || BYTES == 32, "piece size");
+    if constexpr (BYTES == 2) {
+        acc = K_::op(acc, E::widen(__ldg(reinterpret_cast<const unsigned short *>(p))));
+    } else {
+        constexpr int W = BYTES / 4;
+        uint32_t w[W];
+        if constexpr (W == 1) {
+            w[0] = __ldg(reinterpret_cast<const unsigned int *>(p));
+        } else if constexpr (W == 2) {
+            const uint2 t = __ldg(reinterpret_cast<const uint2 *>(p));
+            w[0] = t.x;
+            w[1] = t.y;
+        } else if constexpr (W == 4) {
+            uint32_t (&w4)[4] = w;
+            ld4u(reinterpret_cast<const uint32_t *>(p), w4);
+        } else {
+            uint32_t (&w8)[8] = w;
+            ld8u(reinterpret_cast<const uint32_t *>(p), w8);
+        }
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+            if constexpr (SZ == 4) {
+                acc = K_::op(acc, E::widen(w[k]));
+            } else {
+                acc = K_::op(acc, E::widen(w[k] & 0xffffu));
+                acc = K_::op(acc, E::widen(w[k] >> 16));
+            }
+        }
+    }
+}
+
+// Fold one 32-byte block already loaded as 8 words.
+template <int OP, int DT>
+__device__ __forceinline__ void fold_words(const uint32_t (&w)[8], typename Elem<DT>::A &acc)
+{
+    using E = Elem<DT>;
+    using K_ = Comb<OP, typename E::A>;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        if constexpr (sizeof(typename E::T) == 4) {
+            acc = K_::op(acc, E::widen(w[k]));
+        } else {
+            acc = K_::op(acc, E::widen(w[k] & 0xffffu));
+            acc = K_::op(acc, E::widen(w[k] >> 16));
+        }
+    }
+}
+
+// The unaligned head [b, a) of a span (h = a - b < epb elements, a on a
+// 32-byte boundary) as at most one piece of each power-of-two size, each
+// naturally aligned: sizes ascend with the address.
+template <int OP, int DT>
+__device__ __forceinline__ void fold_head(const typename Elem<DT>::T *pb, int h, typename Elem<DT>::A &acc)
+{
+    if (h & 1)
+        fold_piece<OP, DT, 1>(pb, acc);
+    if (h & 2)
+        fold_piece<OP, DT, 2>(pb + (h & 1), acc);
+    if (h & 4)
+        fold_piece<OP, DT, 4>(pb + (h & 3), acc);
+    if constexpr (epb<DT>() > 8)
+        if (h & 8)
+            fold_piece<OP, DT, 8>(pb + (h & 7), acc);
+}
+
+// The tail [z, e) (t = e - z < epb elements, z on a 32-byte boundary):
+// sizes descend with the address.
+template <int OP, int DT>
+__device__ __forceinline__ void fold_tail(const typename Elem<DT>::T *pz, int t, typename Elem<DT>::A &acc)
+{
+    int o = 0;
+    if constexpr (epb<DT>() > 8) {
+        if (t & 8) {
+            fold_piece<OP, DT, 8>(pz, acc);
+            o = 8;
+        }
+    }
+    if (t & 4) {
+        fold_piece<OP, DT, 4>(pz + o, acc);
+        o += 4;
+    }
+    if (t & 2) {
+        fold_piece<OP, DT, 2>(pz + o, acc);
+        o += 2;
+    }
+    if (t & 1)
+        fold_piece<OP, DT, 1>(pz + o, acc);
+}
+
+// Element index (relative to x) of the first 32-byte boundary at or after
+// element i, for a base x that is element-aligned.
+template <int DT>
+__device__ __forceinline__ int64_t up_to_block(const typename Elem<DT>::T *x, int64_t i)
+{
+    constexpr int SZ = (int)sizeof(typename Elem<DT>::T);
+    const int64_t mis = (int64_t)(((uintptr_t)x & 31u) / SZ);  // x's offset from a boundary, in elements
+    return ((i + mis + epb<DT>() - 1) & ~int64_t(epb<DT>() - 1)) - mis;
+}
+
+template <int DT>
+__device__ __forceinline__ int64_t down_to_block(const typename Elem<DT>::T *x, int64_t i)
+{
+    constexpr int SZ = (int)sizeof(typename Elem<DT>::T);
+    const int64_t mis = (int64_t)(((uintptr_t)x & 31u) / SZ);
+    return ((i + mis) & ~int64_t(epb<DT>() - 1)) - mis;
+}
+
 template <int OP, int DT, int G>
 __global__ void __launch_bounds__(TY_NT)
 typed_rows_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t rows, int64_t len, int accum,
@@ -54,19 +177,34 @@ typed_rows_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t rows, int6
         const bool live = r < rows;
         A acc = K::identity();
         if (live) {
-            const typename E::T *p = x + r * len;
-            int64_t k = gl;
-            for (; k + (TY_U - 1) * G < len; k += TY_U * G) {
-                uint32_t b[TY_U];
+            // Row [b, e): aligned interior [a, z) in 32-byte blocks spread
+            // over the group's lanes (TY_U in flight per lane); head and tail
+            // as naturally aligned pieces by lane 0 and the last lane.  Every
+            // load lies inside the row.
+            const int64_t b = r * len, e = b + len;
+            const int64_t a = up_to_block<DT>(x, b), z = down_to_block<DT>(x, e);
+            if (a <= z) {
+                if (gl == 0)
+                    fold_head<OP, DT>(x + b, (int)(a - b), acc);
+                if (gl == G - 1)
+                    fold_tail<OP, DT>(x + z, (int)(e - z), acc);
+                const int64_t nblk = (z - a) / epb<DT>();
+                const typename E::T *q = x + a;
+                for (int64_t c0 = gl; c0 < nblk; c0 += (int64_t)TY_U * G) {
+                    uint32_t w[TY_U][8];  // all loads out before any fold
 #pragma unroll
-                for (int u = 0; u < TY_U; ++u)
-                    b[u] = load_bits<DT>(p + k + u * G);
+                    for (int u = 0; u < TY_U; ++u)
+                        if (c0 + u * G < nblk)
+                            ld8u(reinterpret_cast<const uint32_t *>(q + (c0 + u * G) * epb<DT>()), w[u]);
 #pragma unroll
-                for (int u = 0; u < TY_U; ++u)
-                    acc = K::op(acc, E::widen(b[u]));
+                    for (int u = 0; u < TY_U; ++u)
+                        if (c0 + u * G < nblk)
+                            fold_words<OP, DT>(w[u], acc);
+                }
+            } else {
+                for (int64_t k = b + gl; k < e; k += G)  // the row inside one block
+                    acc = K::op(acc, E::widen(load_bits<DT>(x + k)));
             }
-            for (; k < len; k += G)
-                acc = K::op(acc, E::widen(load_bits<DT>(p + k)));
             if (accum && gl == 0)
                 acc = K::op(E::widen(bits_of<DT>(out[r])), acc);
         }
@@ -89,18 +227,31 @@ typed_full_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t n, typenam
     const int64_t tid = (int64_t)blockIdx.x * TY_NT + threadIdx.x;
     const int64_t nth = (int64_t)gridDim.x * TY_NT;
     A acc = K::identity();
-    int64_t k = tid;
-    for (; k + (TY_U - 1) * nth < n; k += TY_U * nth) {
-        uint32_t b[TY_U];
+    const int64_t a = up_to_block<DT>(x, 0), z = down_to_block<DT>(x, n);
+    if (a <= z) {
+        // aligned interior as 32-byte blocks, grid-stride, TY_U in flight per
+        // thread; the head and tail pieces by the first and the last thread
+        if (tid == 0)
+            fold_head<OP, DT>(x, (int)a, acc);
+        if (tid == nth - 1)
+            fold_tail<OP, DT>(x + z, (int)(n - z), acc);
+        const int64_t nblk = (z - a) / epb<DT>();
+        const typename E::T *q = x + a;
+        for (int64_t c0 = tid; c0 < nblk; c0 += (int64_t)TY_U * nth) {
+            uint32_t w[TY_U][8];  // all loads out before any fold
 #pragma unroll
-        for (int u = 0; u < TY_U; ++u)
-            b[u] = load_bits<DT>(x + k + u * nth);
+            for (int u = 0; u < TY_U; ++u)
+                if (c0 + u * nth < nblk)
+                    ld8u(reinterpret_cast<const uint32_t *>(q + (c0 + u * nth) * epb<DT>()), w[u]);
 #pragma unroll
-        for (int u = 0; u < TY_U; ++u)
-            acc = K::op(acc, E::widen(b[u]));
+            for (int u = 0; u < TY_U; ++u)
+                if (c0 + u * nth < nblk)
+                    fold_words<OP, DT>(w[u], acc);
+        }
+    } else {
+        for (int64_t k = tid; k < n; k += nth)  // the whole vector inside one block
+            acc = K::op(acc, E::widen(load_bits<DT>(x + k)));
     }
-    for (; k < n; k += nth)
-        acc = K::op(acc, E::widen(load_bits<DT>(x + k)));
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     acc = tree<OP, A, 32>(acc);

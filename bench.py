@@ -517,8 +517,25 @@ def fused_stats(w, stream, per_op, reps=10):
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / reps
     sep = sum(per_op[f"full3 {op}"]["ms"] for op in ("sum", "max", "min") if f"full3 {op}" in per_op)
-    return {"ms": round(ms, 4), "gbs": round(w.bytes_of["full3"] / (ms * 1e-3) / 1e9, 1),
-            "separate_sum_max_min_ms": round(sep, 4), "speedup_vs_separate": round(sep / ms, 3) if sep else None}
+    res = {"ms": round(ms, 4), "gbs": round(w.bytes_of["full3"] / (ms * 1e-3) / 1e9, 1),
+           "separate_sum_max_min_ms": round(sep, 4), "speedup_vs_separate": round(sep / ms, 3) if sep else None}
+    # per-row statistics of the 65536 x 1024 rows, against the three row ops
+    r2, l2 = w.x2.shape
+    ro = torch.empty((r2, 4), device=w.x2.device)
+    for _ in range(2):
+        itr.red_rows_stats(w.x2, ro)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(reps):
+        itr.red_rows_stats(w.x2, ro)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    rms = e0.elapsed_time(e1) / reps
+    rsep = sum(per_op[f"rows2 {op}"]["ms"] for op in ("sum", "max", "min") if f"rows2 {op}" in per_op)
+    res["rows_65536x1024"] = {"ms": round(rms, 4), "gbs": round((4 * r2 * l2 + 16 * r2) / (rms * 1e-3) / 1e9, 1),
+                              "separate_sum_max_min_ms": round(rsep, 4),
+                              "speedup_vs_separate": round(rsep / rms, 3) if rsep else None}
+    return res
 
 
 def supplementary(stream, dev, peak, reps=10):

@@ -130,6 +130,15 @@ int red_full(int op, const float *x, int64_t n, float *out, red_stream_t stream)
 int red_full_stats(const float *x, int64_t n, float *out, red_stream_t stream);
 
 /*
+ * red_rows_stats -- red_full_stats for every row of a row-major fp32 matrix
+ * (row r = x[r*len .. r*len+len)), from one read of x:
+ * out[4r] = sum, out[4r+1] = max, out[4r+2] = min, out[4r+3] = sum of |x|.
+ *   out    device pointer to 4*rows floats, 16-byte aligned.
+ * rows == 0 does nothing; len == 0 returns RED_EINVAL (no max or min).
+ */
+int red_rows_stats(const float *x, int64_t rows, int64_t len, float *out, red_stream_t stream);
+
+/*
  * red_rows -- per-row reduction of a row-major fp32 matrix: row r is
  * x[r*len .. r*len+len), out[r] = op over row r.  With accum != 0 the old
  * value out[r] is folded in as one more operand ([TVM] "How inputs change the

@@ -30,6 +30,7 @@ _SIGNATURES = {
     "red_full": ([_int, _vp, _i64, _vp, _vp], _int),
     "red_full_noalloc": ([_int, _vp, _i64, _vp, _vp], _int),
     "red_full_stats": ([_vp, _i64, _vp, _vp], _int),
+    "red_rows_stats": ([_vp, _i64, _i64, _vp, _vp], _int),
     "red_rows": ([_int, _vp, _i64, _i64, _int, _vp, _vp], _int),
     "red_rows_ragged": ([_int, _vp, _vp, _i64, _i64, _int, _vp, _vp], _int),
     "red_rows_thread": ([_int, _vp, _i64, _int, _int, _vp, _vp], _int),
@@ -128,6 +129,23 @@ def red_full_stats(x: torch.Tensor, out: torch.Tensor | None = None, stream=None
         raise ValueError("out must hold 4 floats")
     with torch.cuda.device(x.device):
         _check(lib().red_full_stats(x.data_ptr(), x.numel(), out.data_ptr(), _stream(stream, x.device)))
+    return out
+
+
+def red_rows_stats(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Per-row (sum, max, min, sum|x|) of a (rows, len) fp32 matrix from one read,
+    into ``out`` of shape (rows, 4)."""
+    _need(x, "x", (torch.float32,))
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D (rows, len)")
+    rows, length = x.shape
+    if out is None:
+        out = torch.empty((rows, 4), dtype=torch.float32, device=x.device)
+    _need(out, "out", (torch.float32,))
+    if out.numel() != 4 * rows:
+        raise ValueError("out must hold 4 floats per row")
+    with torch.cuda.device(x.device):
+        _check(lib().red_rows_stats(x.data_ptr(), rows, length, out.data_ptr(), _stream(stream, x.device)))
     return out
 
 

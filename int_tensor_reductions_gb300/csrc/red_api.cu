@@ -164,6 +164,22 @@ int red_full_stats(const float *x, int64_t n, float *out, red_stream_t stream)
     return launch_full_stats(x, n, out, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int red_rows_stats(const float *x, int64_t rows, int64_t len, float *out, red_stream_t stream)
+{
+    if (rows < 0 || len < 0 || rows > MAX_ELEMS || len > MAX_ELEMS || (len > 0 && rows > MAX_ELEMS / len))
+        return fail(RED_EINVAL, "red_rows_stats: rows = %lld, len = %lld out of range", (long long)rows,
+                    (long long)len);
+    if (rows == 0)
+        return RED_OK;
+    if (len == 0)
+        return fail(RED_EINVAL, "red_rows_stats: empty rows have no max or min");
+    if (!out || misaligned(out, 16))
+        return fail(RED_EINVAL, "red_rows_stats: out is NULL or not 16-byte aligned");
+    if (!x || misaligned(x, 4))
+        return fail(RED_EINVAL, "red_rows_stats: x is NULL or not 4-byte aligned");
+    return launch_rows_stats(x, rows, len, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int red_rows(int op, const float *x, int64_t rows, int64_t len, int accum, float *out, red_stream_t stream)
 {
     if (op < RED_SUM || op > RED_MIN)

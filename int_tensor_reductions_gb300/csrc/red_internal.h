@@ -46,6 +46,7 @@ int launch_full_scratch(int op, const float *x, int64_t n, float *out, cudaStrea
 int launch_rows_split(int op, const float *x, int64_t rows, int64_t len, int accum, float *out,
                       cudaStream_t s, const DeviceInfo &di);
 int launch_full_stats(const float *x, int64_t n, float *out, cudaStream_t s);
+int launch_rows_stats(const float *x, int64_t rows, int64_t len, float *out, cudaStream_t s);
 int launch_rows_thread(int op, const float *x, int64_t rows, int len, int accum, float *out, cudaStream_t s);
 int launch_rows(int op, const float *x, int64_t rows, int64_t len, int accum, float *out,
                 cudaStream_t s);

@@ -1,5 +1,6 @@
-// red_stats.cu -- sum, max, min and sum |x| of one fp32 vector from a single
-// read (the three separate red_full calls read x three times).
+// red_stats.cu -- sum, max, min and sum |x| of one fp32 vector, or of every
+// row of a row-major matrix, from a single read (separate calls read the
+// data once per statistic).
 //
 // Same streaming structure as red_full's kernel: grid-stride 256-bit loads,
 // 4 chunks of 8 in flight per thread, an unaligned head and the tail folded
@@ -49,6 +50,20 @@ struct Stats4 {
         asum.scalar(fabsf(v));
         mx.scalar(v);
         mn.scalar(v);
+    }
+    __device__ __forceinline__ void pair(float2 v)
+    {
+        sum.pair(v);
+        asum.pair(make_float2(fabsf(v.x), fabsf(v.y)));
+        mx.pair(v);
+        mn.pair(v);
+    }
+    __device__ __forceinline__ void quad(float4 v)
+    {
+        sum.quad(v);
+        asum.quad(make_float4(fabsf(v.x), fabsf(v.y), fabsf(v.z), fabsf(v.w)));
+        mx.quad(v);
+        mn.quad(v);
     }
 };
 
@@ -154,7 +169,117 @@ stats_kernel(const float *__restrict__ x, int64_t n, float *__restrict__ part, u
     }
 }
 
+// Per-row statistics: a group of G lanes per row, the row read as its
+// 32-byte aligned interior in 256-bit blocks spread over the lanes (4 in
+// flight per lane) plus its unaligned head and tail as naturally aligned
+// 1-, 2- and 4-float pieces (lane 0 and the last lane), all four folds fed
+// from the one read; out[4r .. 4r+4) = sum, max, min, sum |x|.
+constexpr int SR_NT = 256;
+constexpr int SR_U = 4;
+
+template <int G>
+__global__ void __launch_bounds__(SR_NT)
+rows_stats_kernel(const float *__restrict__ x, int64_t rows, int64_t len, float *__restrict__ out)
+{
+    constexpr int GPW = 32 / G;
+    const int lane = threadIdx.x & 31, gl = lane & (G - 1), gw = lane / G;
+    const int64_t warp = ((int64_t)blockIdx.x * SR_NT + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * SR_NT) >> 5;
+    const int64_t x_mis = (int64_t)(((uintptr_t)x & 31u) >> 2);
+    for (int64_t r0 = warp * GPW; r0 < rows; r0 += nwarps * GPW) {  // warp-uniform
+        const int64_t r = r0 + gw;
+        const bool live = r < rows;
+        Stats4 st;
+        st.init();
+        if (live) {
+            const int64_t b = r * len, e = b + len;
+            const int64_t a = ((b + x_mis + 7) & ~int64_t(7)) - x_mis;
+            const int64_t z = ((e + x_mis) & ~int64_t(7)) - x_mis;
+            if (a <= z) {
+                if (gl == 0) {
+                    const int h = (int)(a - b);
+                    const float *ph = x + b;
+                    if (h & 1)
+                        st.scalar(ld1(ph));
+                    if (h & 2)
+                        st.pair(ld2f(ph + (h & 1)));
+                    if (h & 4)
+                        st.quad(ld4f(ph + (h & 3)));
+                }
+                if (gl == G - 1) {
+                    const int t = (int)(e - z);
+                    const float *pt = x + z;
+                    if (t & 4)
+                        st.quad(ld4f(pt));
+                    if (t & 2)
+                        st.pair(ld2f(pt + (t & 4)));
+                    if (t & 1)
+                        st.scalar(ld1(pt + (t & 6)));
+                }
+                const int64_t nfull = (z - a) >> 3;
+                const float *q = x + a;
+                for (int64_t c0 = gl; c0 < nfull; c0 += (int64_t)SR_U * G) {
+                    float v[SR_U][8];
+#pragma unroll
+                    for (int u = 0; u < SR_U; ++u)
+                        if (c0 + u * G < nfull)
+                            ld8(q + 8 * (c0 + u * G), v[u]);
+#pragma unroll
+                    for (int u = 0; u < SR_U; ++u)
+                        if (c0 + u * G < nfull)
+                            st.chunk(v[u]);
+                }
+            } else {
+                for (int64_t k = b + gl; k < e; k += G)  // the row inside one 32-byte block
+                    st.scalar(ld1(x + k));
+            }
+        }
+        const float s = group_tree<OP_SUM, G>(st.sum.finish());
+        const float m = group_tree<OP_MAX, G>(st.mx.finish());
+        const float n = group_tree<OP_MIN, G>(st.mn.finish());
+        const float a = group_tree<OP_SUM, G>(st.asum.finish());
+        if (live && gl == 0)
+            *reinterpret_cast<float4 *>(out + 4 * r) = make_float4(s, m, n, a);
+    }
+}
+
+template <int G>
+int launch_rows_stats_g(const float *x, int64_t rows, int64_t len, float *out, cudaStream_t s, int sms)
+{
+    static int occ = 0;
+    if (occ == 0)
+        occ = occupancy((const void *)rows_stats_kernel<G>, SR_NT);
+    if (occ <= 0)
+        return fail(RED_ECUDA, "red_rows_stats: kernel cannot be resident on this device");
+    const int64_t rows_per_cta = (int64_t)(SR_NT / 32) * (32 / G);
+    int64_t ctas = (rows + rows_per_cta - 1) / rows_per_cta;
+    if (ctas > (int64_t)sms * occ)
+        ctas = (int64_t)sms * occ;
+    rows_stats_kernel<G><<<(unsigned)ctas, SR_NT, 0, s>>>(x, rows, len, out);
+    count_launches(1);
+    return cuda_fail(cudaGetLastError(), "red_rows_stats launch");
+}
+
 }  // namespace
+
+int launch_rows_stats(const float *x, int64_t rows, int64_t len, float *out, cudaStream_t s)
+{
+    DeviceInfo di;
+    const int st = device_info(&di);
+    if (st != RED_OK)
+        return st;
+    int g = 1;  // about 32 floats per lane
+    while (g < 32 && (int64_t)g * 64 <= len)
+        g *= 2;
+    switch (g) {
+    case 1: return launch_rows_stats_g<1>(x, rows, len, out, s, di.sms);
+    case 2: return launch_rows_stats_g<2>(x, rows, len, out, s, di.sms);
+    case 4: return launch_rows_stats_g<4>(x, rows, len, out, s, di.sms);
+    case 8: return launch_rows_stats_g<8>(x, rows, len, out, s, di.sms);
+    case 16: return launch_rows_stats_g<16>(x, rows, len, out, s, di.sms);
+    default: return launch_rows_stats_g<32>(x, rows, len, out, s, di.sms);
+    }
+}
 
 int launch_full_stats(const float *x, int64_t n, float *out, cudaStream_t s)
 {

@@ -62,3 +62,31 @@ def test_cfg3_4gib_vector():
     _check(x, "cfg3")
     del x
     torch.cuda.empty_cache()
+
+
+def _check_rows(x2d: torch.Tensor, what: str):
+    rows, length = x2d.shape
+    xh = to_host(x2d)
+    got = to_host(itr.red_rows_stats(x2d))
+    s, a = oracle.rows("sum", xh, rows, length)
+    check_sum(got[:, 0], s, a, what + " sum")
+    check_exact(got[:, 1].copy(), oracle.rows("max", xh, rows, length), what + " max")
+    check_exact(got[:, 2].copy(), oracle.rows("min", xh, rows, length), what + " min")
+    check_sum(got[:, 3], a, a, what + " sum|x|")
+
+
+@pytest.mark.parametrize("rows,length", [(1, 1), (5, 7), (33, 8), (100, 24), (257, 41), (64, 1024), (9, 5000)])
+def test_rows_stats_shapes(rows, length):
+    x = synth.uniform((rows * length + 3,), -4.0, 4.0, rows + length, device="cuda")
+    _check_rows(x[:rows * length].view(rows, length), f"{rows}x{length}")
+    _check_rows(x[3:].view(rows, length), f"{rows}x{length} shifted")
+
+
+def test_rows_stats_workload():
+    x, _ = synth.cfg2(device="cuda")
+    _check_rows(x, "65536x1024")
+
+
+def test_rows_stats_rejects_empty_rows():
+    with pytest.raises(itr.RedError):
+        itr.red_rows_stats(torch.empty((3, 0), device="cuda"))

@@ -47,7 +47,7 @@ WORKLOAD = ("all five reduction workloads, one pass of every op: full 2^20 + ful
 DOMINANT = "seg_kernel (red_full, 2^30 fp32 sum/max/min)"
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = [os.path.join(ROOT, "int_tensor_reductions_gb300", "csrc", f)
-                  for f in ("red_full.cu", "red_prims.cuh")]
+                  for f in ("red_full.cu", "red_prims.cuh")] + [os.path.join(ROOT, "include", "red_device.cuh")]
 
 
 def parse_args():
@@ -67,6 +67,8 @@ def parse_args():
                          "colprod4b); for profiling: the line is then not the benchmark's metric")
     ap.add_argument("--scale", type=float, default=1.0,
                     help="fraction of every workload's size (rows / elements); for profiling")
+    ap.add_argument("--case", default="", choices=[""] + sorted(CASES),
+                    help="run one extra library case (not the step) --steps times after --warmup, for profiling")
     return ap.parse_args()
 
 
@@ -171,6 +173,69 @@ def max_over_ranks(x: float, dist=None, device="cpu") -> float:
 def job_gbs(world: int, step_bytes: int, steps: int, max_ms: float) -> float:
     """Whole-job GB/s: every rank processed steps x step_bytes in at most max_ms."""
     return world * step_bytes * steps / (max_ms * 1e-3) / 1e9
+
+
+# ----------------------------------------------------- single extra cases
+
+def _case_inputs(name, dev):
+    """(callable, algorithmic bytes per call) of one extra library case."""
+    import torch
+    import int_tensor_reductions_gb300 as itr
+    from int_tensor_reductions_gb300 import synth
+    if name == "stats_full_2p28":
+        x = synth.normal((1 << 28,), 2, dev)
+        o = torch.empty(4, device=dev)
+        return (lambda: itr.red_full_stats(x, o)), 4 * x.numel() + 16
+    if name == "stats_rows_65536x1024":
+        x, _ = synth.cfg2(dev)
+        o = torch.empty((x.shape[0], 4), device=dev)
+        return (lambda: itr.red_rows_stats(x, o)), 4 * x.numel() + 16 * x.shape[0]
+    if name == "thread_rows_2p22x32":
+        x = synth.normal((1 << 22, 32), 3, dev)
+        o = torch.empty(1 << 22, device=dev)
+        return (lambda: itr.red_rows_thread("sum", x, out=o)), 4 * x.numel() + 4 * x.shape[0]
+    if name == "cols_f16_prod_4096x16384":
+        x = synth.col_input("prod", "f16", (4096, 16384), 11, dev)
+        o = torch.empty(16384, dtype=x.dtype, device=dev)
+        return (lambda: itr.red_cols("prod", x, o)), 2 * x.numel() + 2 * 16384
+    if name == "typed_full_f16_max_2p29":
+        x = synth.col_input("max", "f16", (1 << 29,), 12, dev)
+        o = torch.empty(1, dtype=x.dtype, device=dev)
+        return (lambda: itr.red_full_typed("max", x, o)), 2 * x.numel() + 2
+    if name == "typed_rows_bf16_max_65536x2048":
+        x = synth.col_input("max", "bf16", (65536, 2048), 12, dev)
+        o = torch.empty(65536, dtype=x.dtype, device=dev)
+        return (lambda: itr.red_rows_typed("max", x, out=o)), 2 * x.numel() + 2 * 65536
+    raise KeyError(name)
+
+
+CASES = ("stats_full_2p28", "stats_rows_65536x1024", "thread_rows_2p22x32", "cols_f16_prod_4096x16384",
+         "typed_full_f16_max_2p29", "typed_rows_bf16_max_65536x2048")
+
+
+def run_case(args):
+    """One extra case, --warmup untimed then --steps timed calls (CUDA events);
+    prints one JSON line.  Used for profiling single kernels."""
+    import torch
+    from int_tensor_reductions_gb300 import _build
+    _build.build_lib()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    fn, nbytes = _case_inputs(args.case, dev)
+    for _ in range(max(1, args.warmup)):
+        fn()
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    print(json.dumps({"case": args.case, "ms": round(ms, 5), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                      "bytes_per_call": nbytes}), flush=True)
+    return 0
 
 
 # ------------------------------------------------------------ the workload
@@ -716,6 +781,8 @@ def cpu_baseline(w):
 
 def main():
     args = parse_args()
+    if args.case:
+        return run_case(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

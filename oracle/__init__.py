@@ -43,7 +43,9 @@ def _load():
     global _lib
     if _lib is not None:
         return _lib
-    lib = ctypes.CDLL(build())
+    # ORACLE_LIB: a deliberately broken build of oracle.c, used only by the
+    # test that checks the pins catch planted mistakes
+    lib = ctypes.CDLL(os.environ.get("ORACLE_LIB") or build())
     i64, i32 = ctypes.c_int64, ctypes.c_int
     vp = ctypes.c_void_p
     sigs = {

@@ -151,6 +151,51 @@ def test_ragged_lengths_8_to_40_every_remainder():
     _ragged_case(x, torch.from_numpy(off).cuda(), dst, "lengths 8..40")
 
 
+def _ragged_from_lengths(lens, shift, seed):
+    off = np.zeros(len(lens) + 1, np.int64)
+    off[1:] = np.cumsum(lens)
+    x = synth.uniform((int(off[-1]) + 8,), -4.0, 4.0, seed, device="cuda")[shift:shift + int(off[-1])]
+    dst = synth.uniform((len(lens),), -1.0, 1.0, seed + 1, device="cuda")
+    return x, torch.from_numpy(off).cuda(), dst
+
+
+@pytest.mark.parametrize("g", [0, 2])
+@pytest.mark.parametrize("shift", range(8))
+def test_ragged_every_base_alignment(g, shift):
+    """1000 rows of 8..40 values (several warps' worth of rows, a ragged last
+    iteration) at each of the 8 float offsets of x from a 32-byte boundary;
+    the automatic lanes per row (1) and 2."""
+    itr.red_set_knob(itr.RED_KNOB_RAGGED_GROUP, g)
+    try:
+        lens = np.random.default_rng(60 + shift).integers(8, 41, size=1000)
+        _ragged_case(*_ragged_from_lengths(lens, shift, 61 + shift), f"G={g} shift={shift}")
+    finally:
+        itr.red_set_knob(itr.RED_KNOB_RAGGED_GROUP, 0)
+
+
+@pytest.mark.parametrize("kind", ["all8", "long", "short_rows_sprinkled", "single_row", "huge_row"])
+def test_ragged_shapes(kind):
+    """Rows of exactly 8, rows up to 3000 values, short and empty rows
+    sprinkled among 8..40-value rows, one row, and one 200000-value row, at
+    two base alignments (the L2 prefetch spans round inward at both ends)."""
+    gen = np.random.default_rng(70)
+    if kind == "all8":
+        lens = np.full(1500, 8)
+    elif kind == "long":
+        lens = gen.integers(8, 3000, size=700)
+    elif kind == "short_rows_sprinkled":
+        lens = gen.integers(8, 41, size=128 * 9 + 17)
+        for t in range(0, 10, 2):
+            if 128 * t + 5 < lens.size:
+                lens[128 * t + 5] = t % 8
+    elif kind == "single_row":
+        lens = np.array([37])
+    else:
+        lens = np.array([200_000])
+    for shift in (0, 3):
+        _ragged_case(*_ragged_from_lengths(lens, shift, 71), f"{kind} shift={shift}")
+
+
 def test_ragged_all_empty():
     off = torch.zeros(6, dtype=torch.int64, device="cuda")
     x = torch.empty(0, device="cuda")

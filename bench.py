@@ -519,6 +519,7 @@ def run_ours(args):
         result["full_grid_stage_compare"] = compare_stages(w, stream)
 
     if not args.no_supplementary:
+        result["small_cold_warm"] = small_cold_warm(w, stream)
         result["fused_stats_2p30"] = fused_stats(w, stream, per_op)
         result["supplementary_1gib"] = supplementary(stream, dev, peak)
         result["column_ops"] = column_ops(stream, dev, peak)
@@ -600,6 +601,49 @@ def fused_stats(w, stream, per_op, reps=10):
     res["rows_65536x1024"] = {"ms": round(rms, 4), "gbs": round((4 * r2 * l2 + 16 * r2) / (rms * 1e-3) / 1e9, 1),
                               "separate_sum_max_min_ms": round(rsep, 4),
                               "speedup_vs_separate": round(rsep / rms, 3) if rsep else None}
+    return res
+
+
+def small_cold_warm(w, stream, reps=20):
+    """The two L2-sized workloads (the 2**20 vector, 4 MiB, and the 64 x 65536
+    int32 column product, 16 MiB) timed one call at a time with events around
+    the call alone: warm = repeated calls (the input stays in L2), cold = a
+    write of twice the L2 size before every call.  Before each timed call the
+    GPU is kept busy (a ~25 us device-side sleep when warm, the L2 flush when
+    cold) so that the host's launch latency falls outside the events.  Median
+    and best."""
+    import torch
+    l2 = torch.cuda.get_device_properties(stream.device).L2_cache_size
+    scratch = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=stream.device)
+    res = {"unit": "us", "note": f"single calls, events around the call; cold: {2 * l2 >> 20} MiB written "
+                                 "before each call", "reps": reps}
+    for name in ("full1 sum", "full1 max", "full1 min", "colprod4b i32"):
+        if name not in dict(w.plan):
+            continue
+        fn = w.gpu_call(name)
+        nbytes = w.bytes_of[dict(w.plan)[name]]
+        row = {}
+        for mode in ("warm", "cold"):
+            ts = []
+            for _ in range(3):
+                fn()
+            for _ in range(reps):
+                if mode == "cold":
+                    scratch.fill_(1.0)
+                else:
+                    torch.cuda._sleep(50000)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e3)
+            med = statistics.median(ts)
+            row[mode] = {"median_us": round(med, 2), "best_us": round(min(ts), 2),
+                         "gbs_median": round(nbytes / (med * 1e-6) / 1e9, 1)}
+        res[name] = row
+    del scratch
+    torch.cuda.empty_cache()
     return res
 
 

@@ -31,7 +31,11 @@
  *     aligned and int64 pointers 8-byte aligned; no larger alignment is needed
  *     (the kernels peel an unaligned head and tail off each span).
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
- *     legacy default stream) and never synchronises the host.
+ *     legacy default stream) and never synchronises the host.  Kernels are
+ *     launched with programmatic dependent launch: a library kernel may be
+ *     scheduled onto SMs while the previous kernel on the stream drains, but
+ *     it touches memory only after that kernel has completed and its writes
+ *     are visible, so effects are ordered exactly as in plain stream order.
  *   - Status codes: RED_OK on success.  RED_EINVAL for bad arguments, detected
  *     on the host before anything is launched (nothing is written then).
  *     RED_ECUDA if a CUDA call or launch fails; RED_ENOMEM if the one-time

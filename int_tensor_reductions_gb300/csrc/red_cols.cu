@@ -72,6 +72,7 @@ __global__ void __launch_bounds__(CP_NT, 2)
 cols_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t R, int64_t C, int64_t rows_per_split,
             typename Elem<DT>::A *__restrict__ part, unsigned *__restrict__ tick, typename Elem<DT>::T *__restrict__ out)
 {
+    pdl_enter();
     using E = Elem<DT>;
     using A = typename E::A;
     using K = Comb<OP, A>;
@@ -221,10 +222,10 @@ int launch_cols(const void *xv, int64_t R, int64_t C, void *outv, cudaStream_t s
             return st;
     }
     const dim3 grid((unsigned)tiles, (unsigned)splits);
-    cols_kernel<OP, DT, V><<<grid, CP_NT, 0, s>>>(static_cast<const T *>(xv), R, C, rps, static_cast<A *>(ws.part),
-                                                  ws.tick, static_cast<T *>(outv));
+    const cudaError_t e = launch_pdl(cols_kernel<OP, DT, V>, grid, dim3(CP_NT), s, static_cast<const T *>(xv), R, C,
+                                     rps, static_cast<A *>(ws.part), ws.tick, static_cast<T *>(outv));
     count_launches(1);
-    return cuda_fail(cudaGetLastError(), "red_cols launch");
+    return cuda_fail(e != cudaSuccess ? e : cudaGetLastError(), "red_cols launch");
 }
 
 // Vector width by alignment: 32-byte rows and base -> 256-bit loads,

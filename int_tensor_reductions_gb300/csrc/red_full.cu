@@ -60,6 +60,7 @@ __device__ __forceinline__ void atomic_fold<OP_MIN>(float *addr, float v)
 template <int OP>
 __global__ void fill_identity_kernel(float *out, int64_t n)
 {
+    pdl_enter();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n)
         out[i] = Op<OP>::identity();
@@ -76,6 +77,7 @@ seg_kernel(const float *__restrict__ x, int64_t len, int accum, float *__restric
     __shared__ float s_red[FULL_NT / 32];
     __shared__ int s_last;
 
+    pdl_enter();
     const int64_t seg = blockIdx.y;
     const float *p = x + seg * len;
     const int64_t h = head_to_32B(p, len);
@@ -150,6 +152,7 @@ __global__ void __launch_bounds__(FULL_NT)
 seg_finish_kernel(const float *__restrict__ part, int nparts, int accum, float *__restrict__ out)
 {
     __shared__ float s_red[FULL_NT / 32];
+    pdl_enter();
     const int64_t seg = blockIdx.x;
     float w = Op<OP>::identity();
     for (int i = threadIdx.x; i < nparts; i += FULL_NT)
@@ -174,24 +177,29 @@ int launch_seg(int stage, const float *x, int64_t segs, int64_t len, int splits,
                float *out, const Workspace &ws, cudaStream_t s)
 {
     const dim3 grid((unsigned)splits, (unsigned)segs);
+    cudaError_t e = cudaSuccess;
     if (stage == STAGE_ATOMIC) {
-        fill_identity_kernel<OP><<<(unsigned)((segs + 255) / 256), 256, 0, s>>>(out, segs);
-        seg_kernel<OP, STAGE_ATOMIC><<<grid, FULL_NT, 0, s>>>(x, len, 0, nullptr, nullptr, out);
+        e = launch_pdl(fill_identity_kernel<OP>, dim3((unsigned)((segs + 255) / 256)), dim3(256), s, out, segs);
+        if (e == cudaSuccess)
+            e = launch_pdl(seg_kernel<OP, STAGE_ATOMIC>, grid, dim3(FULL_NT), s, x, len, 0, (float *)nullptr,
+                           (unsigned *)nullptr, out);
         count_launches(2);
     } else if (stage == STAGE_TWO_PASS) {
         float *part = static_cast<float *>(ws.part);
-        seg_kernel<OP, STAGE_TWO_PASS><<<grid, FULL_NT, 0, s>>>(x, len, accum, part, nullptr, out);
+        e = launch_pdl(seg_kernel<OP, STAGE_TWO_PASS>, grid, dim3(FULL_NT), s, x, len, accum, part,
+                       (unsigned *)nullptr, out);
         count_launches(1);
-        if (splits > 1) {
-            seg_finish_kernel<OP><<<(unsigned)segs, FULL_NT, 0, s>>>(part, splits, accum, out);
+        if (e == cudaSuccess && splits > 1) {
+            e = launch_pdl(seg_finish_kernel<OP>, dim3((unsigned)segs), dim3(FULL_NT), s, (const float *)part, splits,
+                           accum, out);
             count_launches(1);
         }
     } else {
-        seg_kernel<OP, STAGE_LAST_BLOCK><<<grid, FULL_NT, 0, s>>>(
-            x, len, accum, static_cast<float *>(ws.part), ws.tick, out);
+        e = launch_pdl(seg_kernel<OP, STAGE_LAST_BLOCK>, grid, dim3(FULL_NT), s, x, len, accum,
+                       static_cast<float *>(ws.part), ws.tick, out);
         count_launches(1);
     }
-    return cuda_fail(cudaGetLastError(), "segmented reduction launch");
+    return cuda_fail(e != cudaSuccess ? e : cudaGetLastError(), "segmented reduction launch");
 }
 
 int launch_seg_op(int op, int stage, const float *x, int64_t segs, int64_t len, int splits, int accum,

@@ -56,6 +56,25 @@ int launch_typed(bool full, int op, int dtype, const void *x, int64_t rows, int6
                  cudaStream_t s);
 int launch_cols(int op, int dtype, const void *x, int64_t R, int64_t C, void *out, cudaStream_t s);
 
+// Kernel launch on stream s with the programmatic-serialization attribute
+// (the kernel's pdl_enter() waits for its predecessors before any global
+// access, so the order of effects is that of a plain launch).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t s, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Resident CTAs per SM of a kernel at `threads` threads and no dynamic shared
 // memory (cached by the callers).
 int occupancy(const void *kernel, int threads);

@@ -27,6 +27,17 @@ namespace red {
 
 enum : int { OP_SUM = 0, OP_MAX = 1, OP_MIN = 2 };
 
+// Programmatic dependent launch: allow the next kernel on the stream to be
+// scheduled now, then wait until every kernel this one depends on has
+// completed and its memory is visible.  Called first in a kernel, so that no
+// global access precedes the wait; both are no-ops for a launch without the
+// programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_enter()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------ packed math
 
 // add.rn.ftz.f32x2 and the three-input max / min live in the public device

@@ -56,6 +56,7 @@ __global__ void __launch_bounds__(ROWS_NT, 3)
 rows_kernel(const float *__restrict__ x, const int64_t *__restrict__ off, int64_t rows, int64_t len,
             int64_t nnz, int accum, float *__restrict__ out)
 {
+    pdl_enter();
     constexpr int GPW = 32 / G;           // rows per warp at a time
     constexpr int U = ROWS_U;              // blocks in flight per lane
     const int64_t x_mis = (int64_t)(((uintptr_t)x & 31u) >> 2);  // x's offset from a 32-byte boundary
@@ -198,9 +199,10 @@ int launch_group(const float *x, const int64_t *off, int64_t rows, int64_t len, 
         ctas = cap;
     if (ctas < 1)
         ctas = 1;
-    rows_kernel<OP, G, RAGGED><<<(unsigned)ctas, ROWS_NT, 0, s>>>(x, off, rows, len, nnz, accum, out);
+    const cudaError_t e = launch_pdl(rows_kernel<OP, G, RAGGED>, dim3((unsigned)ctas), dim3(ROWS_NT), s, x, off, rows,
+                                     len, nnz, accum, out);
     count_launches(1);
-    return cuda_fail(cudaGetLastError(), "row kernel launch");
+    return cuda_fail(e != cudaSuccess ? e : cudaGetLastError(), "row kernel launch");
 }
 
 template <int OP, bool RAGGED>

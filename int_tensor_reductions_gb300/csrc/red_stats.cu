@@ -98,6 +98,7 @@ stats_kernel(const float *__restrict__ x, int64_t n, float *__restrict__ part, u
              float *__restrict__ out)
 {
     __shared__ float sh[4][ST_NW];
+    pdl_enter();
     __shared__ int s_last;
     const int64_t h = head_to_32B(x, n);
     const int64_t nch = (n - h) >> 3;
@@ -181,6 +182,7 @@ template <int G>
 __global__ void __launch_bounds__(SR_NT)
 rows_stats_kernel(const float *__restrict__ x, int64_t rows, int64_t len, float *__restrict__ out)
 {
+    pdl_enter();
     constexpr int GPW = 32 / G;
     const int lane = threadIdx.x & 31, gl = lane & (G - 1), gw = lane / G;
     const int64_t warp = ((int64_t)blockIdx.x * SR_NT + threadIdx.x) >> 5;
@@ -255,9 +257,9 @@ int launch_rows_stats_g(const float *x, int64_t rows, int64_t len, float *out, c
     int64_t ctas = (rows + rows_per_cta - 1) / rows_per_cta;
     if (ctas > (int64_t)sms * occ)
         ctas = (int64_t)sms * occ;
-    rows_stats_kernel<G><<<(unsigned)ctas, SR_NT, 0, s>>>(x, rows, len, out);
+    const cudaError_t e = launch_pdl(rows_stats_kernel<G>, dim3((unsigned)ctas), dim3(SR_NT), s, x, rows, len, out);
     count_launches(1);
-    return cuda_fail(cudaGetLastError(), "red_rows_stats launch");
+    return cuda_fail(e != cudaSuccess ? e : cudaGetLastError(), "red_rows_stats launch");
 }
 
 }  // namespace
@@ -304,9 +306,10 @@ int launch_full_stats(const float *x, int64_t n, float *out, cudaStream_t s)
         if (st != RED_OK)
             return st;
     }
-    stats_kernel<<<(unsigned)ctas, ST_NT, 0, s>>>(x, n, static_cast<float *>(ws.part), ws.tick, out);
+    const cudaError_t e =
+        launch_pdl(stats_kernel, dim3((unsigned)ctas), dim3(ST_NT), s, x, n, static_cast<float *>(ws.part), ws.tick, out);
     count_launches(1);
-    return cuda_fail(cudaGetLastError(), "red_full_stats launch");
+    return cuda_fail(e != cudaSuccess ? e : cudaGetLastError(), "red_full_stats launch");
 }
 
 }  // namespace red

@@ -12,6 +12,7 @@
 // registers.
 #include "red_device.cuh"
 #include "red_internal.h"
+#include "red_prims.cuh"
 #include "red.h"
 
 namespace red {
@@ -25,6 +26,7 @@ thread_rows_kernel(const float *__restrict__ x, int64_t rows, int accum, float *
 {
     constexpr int STRIDE = N | 1;  // odd row stride in shared memory
     __shared__ float s_val[TH_NT * STRIDE];
+    pdl_enter();
     const int64_t r0 = (int64_t)blockIdx.x * TH_NT;
     const int nr = (int)((rows - r0) < TH_NT ? (rows - r0) : TH_NT);
     const float *src = x + r0 * N;
@@ -57,9 +59,9 @@ int launch_n(const float *x, int64_t rows, int accum, float *out, cudaStream_t s
     const int64_t ctas = (rows + TH_NT - 1) / TH_NT;
     if (ctas > 0x7fffffffLL)
         return fail(RED_EINVAL, "red_rows_thread: too many rows");
-    thread_rows_kernel<OP, N><<<(unsigned)ctas, TH_NT, 0, s>>>(x, rows, accum, out);
+    const cudaError_t e = launch_pdl(thread_rows_kernel<OP, N>, dim3((unsigned)ctas), dim3(TH_NT), s, x, rows, accum, out);
     count_launches(1);
-    return cuda_fail(cudaGetLastError(), "red_rows_thread launch");
+    return cuda_fail(e != cudaSuccess ? e : cudaGetLastError(), "red_rows_thread launch");
 }
 
 // Dispatch a runtime length 1..RED_THREAD_MAX_LEN onto the instantiations.

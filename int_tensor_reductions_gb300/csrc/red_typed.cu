@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(TY_NT)
 typed_rows_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t rows, int64_t len, int accum,
                   typename Elem<DT>::T *__restrict__ out)
 {
+    pdl_enter();
     using E = Elem<DT>;
     using A = typename E::A;
     using K = Comb<OP, A>;
@@ -219,6 +220,7 @@ __global__ void __launch_bounds__(TY_NT)
 typed_full_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t n, typename Elem<DT>::A *__restrict__ part,
                   unsigned *__restrict__ tick, typename Elem<DT>::T *__restrict__ out)
 {
+    pdl_enter();
     using E = Elem<DT>;
     using A = typename E::A;
     using K = Comb<OP, A>;
@@ -297,6 +299,7 @@ typed_full_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t n, typenam
 template <int OP, int DT>
 __global__ void typed_fill_kernel(typename Elem<DT>::T *out, int64_t n)
 {
+    pdl_enter();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i < n)
         out[i] = Elem<DT>::narrow(Comb<OP, typename Elem<DT>::A>::identity());
@@ -309,11 +312,12 @@ int typed_rows_dt(const void *xv, int64_t rows, int64_t len, int accum, void *ou
     const T *x = static_cast<const T *>(xv);
     T *out = static_cast<T *>(outv);
     if (len == 0) {
+        cudaError_t e = cudaSuccess;
         if (!accum) {
-            typed_fill_kernel<OP, DT><<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(out, rows);
+            e = launch_pdl(typed_fill_kernel<OP, DT>, dim3((unsigned)((rows + 255) / 256)), dim3(256), s, out, rows);
             count_launches(1);
         }
-        return cuda_fail(cudaGetLastError(), "red_rows_typed launch");
+        return cuda_fail(e != cudaSuccess ? e : cudaGetLastError(), "red_rows_typed launch");
     }
     int g = 1;
     while (g < 32 && (int64_t)g * 32 <= len)
@@ -322,16 +326,18 @@ int typed_rows_dt(const void *xv, int64_t rows, int64_t len, int accum, void *ou
     int64_t ctas = (rows + rows_per_cta - 1) / rows_per_cta;
     if (ctas > (int64_t)sms * 8)
         ctas = (int64_t)sms * 8;
+    const dim3 grid((unsigned)ctas), block(TY_NT);
+    cudaError_t e;
     switch (g) {
-    case 1: typed_rows_kernel<OP, DT, 1><<<(unsigned)ctas, TY_NT, 0, s>>>(x, rows, len, accum, out); break;
-    case 2: typed_rows_kernel<OP, DT, 2><<<(unsigned)ctas, TY_NT, 0, s>>>(x, rows, len, accum, out); break;
-    case 4: typed_rows_kernel<OP, DT, 4><<<(unsigned)ctas, TY_NT, 0, s>>>(x, rows, len, accum, out); break;
-    case 8: typed_rows_kernel<OP, DT, 8><<<(unsigned)ctas, TY_NT, 0, s>>>(x, rows, len, accum, out); break;
-    case 16: typed_rows_kernel<OP, DT, 16><<<(unsigned)ctas, TY_NT, 0, s>>>(x, rows, len, accum, out); break;
-    default: typed_rows_kernel<OP, DT, 32><<<(unsigned)ctas, TY_NT, 0, s>>>(x, rows, len, accum, out); break;
+    case 1: e = launch_pdl(typed_rows_kernel<OP, DT, 1>, grid, block, s, x, rows, len, accum, out); break;
+    case 2: e = launch_pdl(typed_rows_kernel<OP, DT, 2>, grid, block, s, x, rows, len, accum, out); break;
+    case 4: e = launch_pdl(typed_rows_kernel<OP, DT, 4>, grid, block, s, x, rows, len, accum, out); break;
+    case 8: e = launch_pdl(typed_rows_kernel<OP, DT, 8>, grid, block, s, x, rows, len, accum, out); break;
+    case 16: e = launch_pdl(typed_rows_kernel<OP, DT, 16>, grid, block, s, x, rows, len, accum, out); break;
+    default: e = launch_pdl(typed_rows_kernel<OP, DT, 32>, grid, block, s, x, rows, len, accum, out); break;
     }
     count_launches(1);
-    return cuda_fail(cudaGetLastError(), "red_rows_typed launch");
+    return cuda_fail(e != cudaSuccess ? e : cudaGetLastError(), "red_rows_typed launch");
 }
 
 template <int OP, int DT>
@@ -342,9 +348,9 @@ int typed_full_dt(const void *xv, int64_t n, void *outv, cudaStream_t s, int sms
     const T *x = static_cast<const T *>(xv);
     T *out = static_cast<T *>(outv);
     if (n == 0) {
-        typed_fill_kernel<OP, DT><<<1, 32, 0, s>>>(out, 1);
+        const cudaError_t e = launch_pdl(typed_fill_kernel<OP, DT>, dim3(1), dim3(32), s, out, (int64_t)1);
         count_launches(1);
-        return cuda_fail(cudaGetLastError(), "red_full_typed launch");
+        return cuda_fail(e != cudaSuccess ? e : cudaGetLastError(), "red_full_typed launch");
     }
     static int occ = 0;
     if (occ == 0)
@@ -363,9 +369,10 @@ int typed_full_dt(const void *xv, int64_t n, void *outv, cudaStream_t s, int sms
         if (st != RED_OK)
             return st;
     }
-    typed_full_kernel<OP, DT><<<(unsigned)ctas, TY_NT, 0, s>>>(x, n, static_cast<A *>(ws.part), ws.tick, out);
+    const cudaError_t e = launch_pdl(typed_full_kernel<OP, DT>, dim3((unsigned)ctas), dim3(TY_NT), s, x, n,
+                                     static_cast<A *>(ws.part), ws.tick, out);
     count_launches(1);
-    return cuda_fail(cudaGetLastError(), "red_full_typed launch");
+    return cuda_fail(e != cudaSuccess ? e : cudaGetLastError(), "red_full_typed launch");
 }
 
 template <int OP>

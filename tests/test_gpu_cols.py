@@ -104,6 +104,17 @@ def test_forced_row_splits(dtype, splits):
         itr.red_set_knob(itr.RED_KNOB_COLPROD_SPLITS, 0)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "i32", "f16", "u16"])
+@pytest.mark.parametrize("R,C", [(5000, 256), (2000, 8192), (777, 33000), (65, 40000), (3, 70000)])
+def test_tall_wide_and_ragged_tiles(R, C, dtype):
+    """One column tile of 5000 rows, 32 tiles of 2000 rows, 129 tiles with a
+    ragged last one, and very wide matrices of few rows (many tiles, few or
+    no row splits)."""
+    for op in ("prod", "sum", "max"):
+        x = synth.col_input(op, dtype, (R, C), R + C, device="cuda")
+        check_cols(op, dtype, x, f"{op} {dtype} {R}x{C}")
+
+
 def test_int_wrap_closed_forms():
     for c, R, dtype, ref in [(2, 15, "i16", -32768), (2, 16, "i16", 0), (3, 11, "i16", 177147 - 3 * 65536),
                              (3, 11, "u16", 177147 % 65536), (2, 32, "u32", 0), (3, 21, "u32", 3**21 % 2**32),

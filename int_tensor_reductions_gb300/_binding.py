@@ -99,9 +99,19 @@ def _stream(stream, device) -> int:
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
-def _need(t: torch.Tensor, name: str, dtypes):
+def _need(t: torch.Tensor, name: str, dtypes, like: torch.Tensor | None = None, min_numel: int = 0):
+    """t is a contiguous CUDA tensor of one of ``dtypes`` (None: any), on
+    ``like``'s device when given, with at least ``min_numel`` elements."""
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if like is not None and t.device != like.device:
+        raise ValueError(f"{name} is on {t.device}, x on {like.device}")
+    if t.numel() < min_numel:
+        raise ValueError(f"{name} must hold at least {min_numel} element(s)")
+    if dtypes is None:
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        return
     if t.dtype not in dtypes:
         raise ValueError(f"{name} must have dtype {dtypes}, got {t.dtype}")
     if not t.is_contiguous():
@@ -113,7 +123,7 @@ def red_full(op, x: torch.Tensor, out: torch.Tensor | None = None, stream=None) 
     _need(x, "x", (torch.float32,))
     if out is None:
         out = torch.empty(1, dtype=torch.float32, device=x.device)
-    _need(out, "out", (torch.float32,))
+    _need(out, "out", (torch.float32,), x, 1)
     with torch.cuda.device(x.device):
         _check(lib().red_full(_op(op), x.data_ptr(), x.numel(), out.data_ptr(), _stream(stream, x.device)))
     return out
@@ -124,9 +134,7 @@ def red_full_stats(x: torch.Tensor, out: torch.Tensor | None = None, stream=None
     _need(x, "x", (torch.float32,))
     if out is None:
         out = torch.empty(4, dtype=torch.float32, device=x.device)
-    _need(out, "out", (torch.float32,))
-    if out.numel() < 4:
-        raise ValueError("out must hold 4 floats")
+    _need(out, "out", (torch.float32,), x, 4)
     with torch.cuda.device(x.device):
         _check(lib().red_full_stats(x.data_ptr(), x.numel(), out.data_ptr(), _stream(stream, x.device)))
     return out
@@ -141,7 +149,7 @@ def red_rows_stats(x: torch.Tensor, out: torch.Tensor | None = None, stream=None
     rows, length = x.shape
     if out is None:
         out = torch.empty((rows, 4), dtype=torch.float32, device=x.device)
-    _need(out, "out", (torch.float32,))
+    _need(out, "out", (torch.float32,), x)
     if out.numel() != 4 * rows:
         raise ValueError("out must hold 4 floats per row")
     with torch.cuda.device(x.device):
@@ -155,7 +163,7 @@ def red_full_noalloc(op, x: torch.Tensor, out: torch.Tensor, stream=None) -> tor
     cudaMalloc).  ``out`` must be given, so this wrapper allocates nothing
     either."""
     _need(x, "x", (torch.float32,))
-    _need(out, "out", (torch.float32,))
+    _need(out, "out", (torch.float32,), x, 1)
     with torch.cuda.device(x.device):
         _check(lib().red_full_noalloc(_op(op), x.data_ptr(), x.numel(), out.data_ptr(),
                                       _stream(stream, x.device)))
@@ -173,7 +181,7 @@ def red_rows(op, x: torch.Tensor, accum: bool = False, out: torch.Tensor | None 
         if accum:
             raise ValueError("accum needs an existing out")
         out = torch.empty(rows, dtype=torch.float32, device=x.device)
-    _need(out, "out", (torch.float32,))
+    _need(out, "out", (torch.float32,), x)
     if out.numel() != rows:
         raise ValueError("out must have one element per row")
     with torch.cuda.device(x.device):
@@ -194,7 +202,7 @@ def red_rows_thread(op, x: torch.Tensor, accum: bool = False, out: torch.Tensor 
         if accum:
             raise ValueError("accum needs an existing out")
         out = torch.empty(rows, dtype=torch.float32, device=x.device)
-    _need(out, "out", (torch.float32,))
+    _need(out, "out", (torch.float32,), x)
     if out.numel() != rows:
         raise ValueError("out must have one element per row")
     with torch.cuda.device(x.device):
@@ -207,7 +215,7 @@ def red_rows_ragged(op, x: torch.Tensor, offsets: torch.Tensor, accum: bool = Fa
                     out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Per-row reduction of packed rows x[offsets[r]:offsets[r+1]]."""
     _need(x, "x", (torch.float32,))
-    _need(offsets, "offsets", (torch.int64,))
+    _need(offsets, "offsets", (torch.int64,), x, 1)
     rows = offsets.numel() - 1
     if rows < 0:
         raise ValueError("offsets needs rows + 1 entries")
@@ -215,7 +223,7 @@ def red_rows_ragged(op, x: torch.Tensor, offsets: torch.Tensor, accum: bool = Fa
         if accum:
             raise ValueError("accum needs an existing out")
         out = torch.empty(rows, dtype=torch.float32, device=x.device)
-    _need(out, "out", (torch.float32,))
+    _need(out, "out", (torch.float32,), x)
     if out.numel() != rows:
         raise ValueError("out must have one element per row")
     with torch.cuda.device(x.device):
@@ -247,8 +255,9 @@ def red_cols(op, x: torch.Tensor, out: torch.Tensor | None = None, stream=None, 
     R, C = x.shape
     if out is None:
         out = torch.empty(C, dtype=x.dtype, device=x.device)
-    if not out.is_cuda or not out.is_contiguous() or out.element_size() != x.element_size():
-        raise ValueError("out must be a contiguous CUDA tensor of x's element size")
+    _need(out, "out", None, x)
+    if out.element_size() != x.element_size():
+        raise ValueError("out must have x's element size")
     if out.numel() != C:
         raise ValueError("out must have C elements")
     with torch.cuda.device(x.device):
@@ -264,8 +273,9 @@ def red_full_typed(op, x: torch.Tensor, out: torch.Tensor | None = None, stream=
     code = _col_dtype(x, dtype)
     if out is None:
         out = torch.empty(1, dtype=x.dtype, device=x.device)
-    if not out.is_cuda or out.element_size() != x.element_size():
-        raise ValueError("out must be a CUDA tensor of x's element size")
+    _need(out, "out", None, x, 1)
+    if out.element_size() != x.element_size():
+        raise ValueError("out must have x's element size")
     with torch.cuda.device(x.device):
         _check(lib().red_full_typed(_op(op), code, x.data_ptr(), x.numel(), out.data_ptr(),
                                     _stream(stream, x.device)))
@@ -286,8 +296,9 @@ def red_rows_typed(op, x: torch.Tensor, accum: bool = False, out: torch.Tensor |
         if accum:
             raise ValueError("accum needs an existing out")
         out = torch.empty(rows, dtype=x.dtype, device=x.device)
-    if not out.is_cuda or not out.is_contiguous() or out.element_size() != x.element_size():
-        raise ValueError("out must be a contiguous CUDA tensor of x's element size")
+    _need(out, "out", None, x)
+    if out.element_size() != x.element_size():
+        raise ValueError("out must have x's element size")
     if out.numel() != rows:
         raise ValueError("out must have one element per row")
     with torch.cuda.device(x.device):
@@ -307,8 +318,9 @@ def red_colprod(x: torch.Tensor, out: torch.Tensor | None = None, stream=None, d
     R, C = x.shape
     if out is None:
         out = torch.empty(C, dtype=x.dtype, device=x.device)
-    if not out.is_cuda or not out.is_contiguous() or out.element_size() != x.element_size():
-        raise ValueError("out must be a contiguous CUDA tensor of x's element size")
+    _need(out, "out", None, x)
+    if out.element_size() != x.element_size():
+        raise ValueError("out must have x's element size")
     if out.numel() != C:
         raise ValueError("out must have C elements")
     with torch.cuda.device(x.device):

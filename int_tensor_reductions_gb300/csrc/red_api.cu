@@ -18,7 +18,7 @@ constexpr int64_t MAX_ELEMS = int64_t(1) << 44;  // guards index arithmetic
 thread_local char g_err[512] = "";
 std::mutex g_mu;
 Workspace g_ws[MAX_DEVICES];
-int g_sms[MAX_DEVICES];
+std::atomic<int> g_sms[MAX_DEVICES];
 
 std::atomic<int> g_full_mode{RED_MODE_AUTO};
 std::atomic<uint64_t> g_launches{0};
@@ -55,15 +55,15 @@ int device_info(DeviceInfo *info)
         return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= MAX_DEVICES)
         return fail(RED_ECUDA, "device ordinal %d out of range", dev);
-    if (g_sms[dev] == 0) {
-        int sms = 0;
+    int sms = g_sms[dev].load(std::memory_order_relaxed);
+    if (sms == 0) {
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess)
             return cuda_fail(e, "cudaDeviceGetAttribute");
-        g_sms[dev] = sms;
+        g_sms[dev].store(sms, std::memory_order_relaxed);
     }
     info->dev = dev;
-    info->sms = g_sms[dev];
+    info->sms = sms;
     return RED_OK;
 }
 

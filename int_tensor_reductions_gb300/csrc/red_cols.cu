@@ -166,9 +166,8 @@ int launch_cols(const void *xv, int64_t R, int64_t C, void *outv, cudaStream_t s
     using E = Elem<DT>;
     using T = typename E::T;
     using A = typename E::A;
-    static int occ = 0;
-    if (occ == 0)
-        occ = occupancy((const void *)cols_kernel<OP, DT, V>, CP_NT);
+    static std::atomic<int> occ_cache{0};
+    const int occ = cached_occupancy(occ_cache, (const void *)cols_kernel<OP, DT, V>, CP_NT);
     if (occ <= 0)
         return fail(RED_ECUDA, "red_cols: kernel cannot be resident on this device");
     constexpr int U = sizeof(T) == 4 ? 4 : 2;

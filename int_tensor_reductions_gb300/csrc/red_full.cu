@@ -165,10 +165,8 @@ seg_finish_kernel(const float *__restrict__ part, int nparts, int accum, float *
 template <int OP, int STAGE>
 int seg_occupancy()
 {
-    static int occ = 0;
-    if (occ == 0)
-        occ = occupancy((const void *)seg_kernel<OP, STAGE>, FULL_NT);
-    return occ;
+    static std::atomic<int> occ_cache{0};
+    return cached_occupancy(occ_cache, (const void *)seg_kernel<OP, STAGE>, FULL_NT);
 }
 
 // Launch the segmented reduction with `splits` CTAs per segment.

@@ -3,6 +3,7 @@
 // the kernel launchers behind the C entry points.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -76,7 +77,21 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStre
 }
 
 // Resident CTAs per SM of a kernel at `threads` threads and no dynamic shared
-// memory (cached by the callers).
+// memory; 0 if the query fails.
 int occupancy(const void *kernel, int threads);
+
+// occupancy() cached in `cache` (one per kernel instantiation) after the
+// first successful query; concurrent first calls may both query, which is
+// harmless, and a failed query is not cached.
+inline int cached_occupancy(std::atomic<int> &cache, const void *kernel, int threads)
+{
+    int v = cache.load(std::memory_order_relaxed);
+    if (v <= 0) {
+        v = occupancy(kernel, threads);
+        if (v > 0)
+            cache.store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
 
 }  // namespace red

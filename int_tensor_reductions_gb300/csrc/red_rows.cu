@@ -187,9 +187,8 @@ template <int OP, int G, bool RAGGED>
 int launch_group(const float *x, const int64_t *off, int64_t rows, int64_t len, int64_t nnz, int accum,
                  float *out, cudaStream_t s, int sms)
 {
-    static int occ = 0;
-    if (occ == 0)
-        occ = occupancy((const void *)rows_kernel<OP, G, RAGGED>, ROWS_NT);
+    static std::atomic<int> occ_cache{0};
+    const int occ = cached_occupancy(occ_cache, (const void *)rows_kernel<OP, G, RAGGED>, ROWS_NT);
     if (occ <= 0)
         return fail(RED_ECUDA, "row kernel cannot be resident on this device");
     const int64_t rows_per_cta = (int64_t)(ROWS_NT / 32) * (32 / G);

@@ -248,9 +248,8 @@ rows_stats_kernel(const float *__restrict__ x, int64_t rows, int64_t len, float 
 template <int G>
 int launch_rows_stats_g(const float *x, int64_t rows, int64_t len, float *out, cudaStream_t s, int sms)
 {
-    static int occ = 0;
-    if (occ == 0)
-        occ = occupancy((const void *)rows_stats_kernel<G>, SR_NT);
+    static std::atomic<int> occ_cache{0};
+    const int occ = cached_occupancy(occ_cache, (const void *)rows_stats_kernel<G>, SR_NT);
     if (occ <= 0)
         return fail(RED_ECUDA, "red_rows_stats: kernel cannot be resident on this device");
     const int64_t rows_per_cta = (int64_t)(SR_NT / 32) * (32 / G);
@@ -289,9 +288,8 @@ int launch_full_stats(const float *x, int64_t n, float *out, cudaStream_t s)
     int st = device_info(&di);
     if (st != RED_OK)
         return st;
-    static int occ = 0;
-    if (occ == 0)
-        occ = occupancy((const void *)stats_kernel, ST_NT);
+    static std::atomic<int> occ_cache{0};
+    const int occ = cached_occupancy(occ_cache, (const void *)stats_kernel, ST_NT);
     if (occ <= 0)
         return fail(RED_ECUDA, "red_full_stats: kernel cannot be resident on this device");
     const int64_t want = (n / 8 + 1 + (int64_t)ST_NT * ST_U - 1) / ((int64_t)ST_NT * ST_U);

@@ -352,9 +352,8 @@ int typed_full_dt(const void *xv, int64_t n, void *outv, cudaStream_t s, int sms
         count_launches(1);
         return cuda_fail(e != cudaSuccess ? e : cudaGetLastError(), "red_full_typed launch");
     }
-    static int occ = 0;
-    if (occ == 0)
-        occ = occupancy((const void *)typed_full_kernel<OP, DT>, TY_NT);
+    static std::atomic<int> occ_cache{0};
+    const int occ = cached_occupancy(occ_cache, (const void *)typed_full_kernel<OP, DT>, TY_NT);
     if (occ <= 0)
         return fail(RED_ECUDA, "red_full_typed: kernel cannot be resident on this device");
     const int64_t want = (n + (int64_t)TY_NT * TY_U - 1) / ((int64_t)TY_NT * TY_U);

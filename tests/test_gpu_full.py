@@ -116,3 +116,17 @@ def test_cfg3_4gib_vector(cfg3, mode):
     check_sum(to_host(itr.red_full("sum", x)), s, a, f"cfg3 sum mode {mode}")
     check_exact(to_host(itr.red_full("max", x)), np.array([ref["max"]], np.float32), "cfg3 max")
     check_exact(to_host(itr.red_full("min", x)), np.array([ref["min"]], np.float32), "cfg3 min")
+
+
+def test_binding_rejects_short_buffers():
+    """The Python wrappers check buffer sizes the C ABI cannot see (it takes
+    plain pointers): an empty out, or offsets without rows + 1 entries, is a
+    ValueError before anything is launched."""
+    x = torch.ones(100, device="cuda")
+    e = torch.empty(0, device="cuda")
+    for call in (lambda: itr.red_full("sum", x, e), lambda: itr.red_full_noalloc("sum", x, e),
+                 lambda: itr.red_full_typed("sum", x, e), lambda: itr.red_full_stats(x, torch.empty(3, device="cuda")),
+                 lambda: itr.red_rows_ragged("sum", x, torch.empty(0, dtype=torch.int64, device="cuda")),
+                 lambda: itr.red_rows("sum", x.view(10, 10), out=torch.empty(9, device="cuda"))):
+        with pytest.raises(ValueError):
+            call()

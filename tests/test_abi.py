@@ -104,3 +104,15 @@ def test_binding_refuses_cpu_tensors():
     import int_tensor_reductions_gb300 as itr
     with pytest.raises(ValueError):
         itr.red_full("sum", torch.ones(8))
+
+
+def test_c_client_compiles_and_links(lib, tmp_path):
+    """tests/c/red_c_client.c (run on the GPU by test_gpu_c_client.py) builds
+    against red.h as C99 and links against libred.so and the CUDA runtime."""
+    import subprocess
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    pkg = os.path.dirname(lib._name)
+    subprocess.run(["gcc", "-std=c99", "-O2", "-Wall", "-Wextra", "-Werror", "-I" + os.path.join(ROOT, "include"),
+                    "-I" + os.path.join(cuda, "include"), os.path.join(ROOT, "tests", "c", "red_c_client.c"),
+                    "-o", str(tmp_path / "client"), "-L" + pkg, "-lred", "-L" + os.path.join(cuda, "lib64"),
+                    "-lcudart"], check=True)

@@ -496,7 +496,8 @@ def run_ours(args):
             "bytes_per_step": w.step_bytes,
             "l2": "inputs larger than L2 between reuses: ops interleaved so every buffer is re-read only "
                   "after >= 4 GiB of other reads (L2 is 126 MiB)",
-            "full_grid_stage": {1: "two-pass", 2: "last-block", 3: "atomic"}[itr.red_get_full_mode()],
+            "full_grid_stage": {0: "auto: two-pass for sum, atomic for max/min", 1: "two-pass", 2: "last-block",
+                                3: "atomic"}[itr.red_get_full_mode()],
             "parallelism": f"replicas x{world}",
         },
         "frac_of_nominal_8TBs": round(value / world / NOMINAL_HBM_GBS, 4),
@@ -604,44 +605,50 @@ def fused_stats(w, stream, per_op, reps=10):
     return res
 
 
-def small_cold_warm(w, stream, reps=20):
+def small_cold_warm(w, stream, calls=20, reps=50):
     """The two L2-sized workloads (the 2**20 vector, 4 MiB, and the 64 x 65536
-    int32 column product, 16 MiB) timed one call at a time with events around
-    the call alone: warm = repeated calls (the input stays in L2), cold = a
-    write of twice the L2 size before every call.  Before each timed call the
-    GPU is kept busy (a ~25 us device-side sleep when warm, the L2 flush when
-    cold) so that the host's launch latency falls outside the events.  Median
-    and best."""
+    int32 column product, 16 MiB), per call.  Single calls are too short for
+    CUDA events (their timestamps step by ~2 us), so the calls are captured
+    in CUDA graphs and each graph is replayed ``reps`` times between two
+    events: warm = ``calls`` back-to-back calls (the input stays in L2) per
+    replay; cold = ``calls`` pairs of (write twice the L2 size, call) minus
+    the same graph without the calls."""
     import torch
     l2 = torch.cuda.get_device_properties(stream.device).L2_cache_size
     scratch = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=stream.device)
-    res = {"unit": "us", "note": f"single calls, events around the call; cold: {2 * l2 >> 20} MiB written "
-                                 "before each call", "reps": reps}
+
+    def per_replay(body):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            body()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps  # us
+
+    res = {"unit": "us", "note": f"per call, from CUDA-graph replays ({calls} calls per graph, {reps} replays); "
+                                 f"cold: {2 * l2 >> 20} MiB written before each call, that write's own time "
+                                 "subtracted"}
+    flushes = per_replay(lambda: [scratch.fill_(1.0) for _ in range(calls)])
     for name in ("full1 sum", "full1 max", "full1 min", "colprod4b i32"):
         if name not in dict(w.plan):
             continue
         fn = w.gpu_call(name)
         nbytes = w.bytes_of[dict(w.plan)[name]]
-        row = {}
-        for mode in ("warm", "cold"):
-            ts = []
-            for _ in range(3):
-                fn()
-            for _ in range(reps):
-                if mode == "cold":
-                    scratch.fill_(1.0)
-                else:
-                    torch.cuda._sleep(50000)
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                fn()
-                e1.record(stream)
-                e1.synchronize()
-                ts.append(e0.elapsed_time(e1) * 1e3)
-            med = statistics.median(ts)
-            row[mode] = {"median_us": round(med, 2), "best_us": round(min(ts), 2),
-                         "gbs_median": round(nbytes / (med * 1e-6) / 1e9, 1)}
-        res[name] = row
+        fn()
+        torch.cuda.synchronize()
+        warm = per_replay(lambda: [fn() for _ in range(calls)]) / calls
+        both = per_replay(lambda: [(scratch.fill_(1.0), fn()) for _ in range(calls)])
+        cold = (both - flushes) / calls
+        res[name] = {"warm_us": round(warm, 2), "cold_us": round(cold, 2),
+                     "warm_gbs": round(nbytes / (warm * 1e-6) / 1e9, 1),
+                     "cold_gbs": round(nbytes / (cold * 1e-6) / 1e9, 1)}
     del scratch
     torch.cuda.empty_cache()
     return res

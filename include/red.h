@@ -91,7 +91,8 @@ enum red_status { RED_OK = 0, RED_EINVAL = -1, RED_ECUDA = -2, RED_ENOMEM = -3 }
 
 /* Grid stage of red_full (how the per-CTA partials become one scalar). */
 enum red_full_mode {
-    RED_MODE_AUTO = 0,       /* the measured default */
+    RED_MODE_AUTO = 0,       /* the measured default: two-pass for sums (deterministic),
+                                atomic for max / min (exact in any order) */
     RED_MODE_TWO_PASS = 1,   /* partials to the workspace, then a second kernel */
     RED_MODE_LAST_BLOCK = 2, /* one kernel; the last CTA to finish folds the partials */
     RED_MODE_ATOMIC = 3      /* identity into *out, then one atomic per CTA */
@@ -281,7 +282,7 @@ int red_full_noalloc(int op, const float *x, int64_t n, float *out, red_stream_t
  * Returns RED_OK, or RED_EINVAL for an unknown mode. */
 int red_set_full_mode(int mode);
 
-/* The grid stage red_full uses now (never RED_MODE_AUTO: the resolved one). */
+/* The current setting of red_set_full_mode (RED_MODE_AUTO by default). */
 int red_get_full_mode(void);
 
 /* Set a tuning knob (enum red_knob); value 0 restores the automatic choice.

@@ -24,8 +24,6 @@ std::atomic<int> g_full_mode{RED_MODE_AUTO};
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_knobs[8];
 
-// Grid stage used when the mode is RED_MODE_AUTO.
-constexpr int AUTO_FULL_STAGE = RED_MODE_LAST_BLOCK;
 
 bool misaligned(const void *p, uintptr_t a) { return ((uintptr_t)p) % a != 0; }
 
@@ -112,10 +110,18 @@ int knob(int which)
 
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
-int full_mode()
+int full_stage(int op)
 {
+    // Automatic choice, by measurement (the three stages tie on inputs far
+    // larger than L2; on small ones a second launch, overlapped by
+    // programmatic dependent launch, costs less than the last-block fence
+    // and partials read, and one atomic per CTA less than either): sums take
+    // the two-pass stage, which is deterministic; max / min the atomic stage,
+    // exact in any order.
     const int m = g_full_mode.load(std::memory_order_relaxed);
-    return m == RED_MODE_AUTO ? AUTO_FULL_STAGE : m;
+    if (m != RED_MODE_AUTO)
+        return m;
+    return op == RED_SUM ? RED_MODE_TWO_PASS : RED_MODE_ATOMIC;
 }
 
 int occupancy(const void *kernel, int threads)
@@ -318,7 +324,7 @@ int red_set_full_mode(int mode)
     return RED_OK;
 }
 
-int red_get_full_mode(void) { return full_mode(); }
+int red_get_full_mode(void) { return g_full_mode.load(std::memory_order_relaxed); }
 
 int red_set_knob(int k, int value)
 {

@@ -238,7 +238,7 @@ int launch_full(int op, const float *x, int64_t n, float *out, cudaStream_t s)
     int st = device_info(&di);
     if (st != RED_OK)
         return st;
-    const int stage = full_mode();
+    int stage = full_stage(op);
     const int occ = ctas_per_sm(op, stage);
     if (occ <= 0)
         return fail(RED_ECUDA, "red_full: kernel cannot be resident on this device");
@@ -250,6 +250,8 @@ int launch_full(int op, const float *x, int64_t n, float *out, cudaStream_t s)
         ctas = want;
     if (ctas < 1)
         ctas = 1;
+    if (ctas == 1)
+        stage = STAGE_LAST_BLOCK;  // one CTA writes the result itself: no grid stage, one launch
     Workspace ws;
     if (stage != STAGE_ATOMIC && ctas > 1) {
         st = get_workspace(&ws);

@@ -36,7 +36,7 @@ int get_workspace(Workspace *ws);
 
 int knob(int which);        // 0 = automatic
 void count_launches(int n); // adds n to red_launch_count()
-int full_mode();            // resolved grid stage of red_full (1, 2 or 3)
+int full_stage(int op);    // grid stage red_full uses for op (1, 2 or 3)
 
 // Launchers: arguments have been validated by the entry points.
 int launch_full(int op, const float *x, int64_t n, float *out, cudaStream_t s);

@@ -59,6 +59,14 @@ MUTANTS = {
                                            "        if (0)\n            return ORC_EINVAL;"),
     "full min keeps the first element": ("        if (x[i] < m)\n            m = x[i];\n    *out = m;",
                                          "        if (x[i] < m && 0)\n            m = x[i];\n    *out = m;"),
+    "column fold drops the last row": ("        for (int64_t i = 1; i < R; ++i) {\n            const double v = elem_f(x, dtype, i * C + j);",
+                                       "        for (int64_t i = 1; i < R - 1; ++i) {\n            const double v = elem_f(x, dtype, i * C + j);"),
+    "full sum|x| forgets the absolute value": ("        a += fabs((double)x[i]);\n    }\n    *sum = s;",
+                                               "        a += (double)x[i];\n    }\n    *sum = s;"),
+    "empty typed product row starts from 0": ("acc = op == ORC_PROD ? 1.0 : 0.0;", "acc = 0.0;"),
+    "half subnormals decoded with a wrong scale": ("v = ldexp((double)f, -24);", "v = ldexp((double)f, -25);"),
+    "short thread fold adds accum last": ("        float r = a[0];\n        if (accum)\n            r = r + dst;\n        for (int64_t i = 1; i < n; ++i)\n            r = r + a[i];\n        return r;",
+                                          "        float r = a[0];\n        for (int64_t i = 1; i < n; ++i)\n            r = r + a[i];\n        if (accum)\n            r = r + dst;\n        return r;"),
     "half decode uses a wrong exponent bias": ("v = ldexp((double)(f | 0x400), e - 25);", "v = ldexp((double)(f | 0x400), e - 24);"),
 }
 

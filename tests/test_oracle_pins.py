@@ -490,6 +490,11 @@ def test_rows_typed_accum_and_empty():
     assert oracle.rows_typed("sum", "i32", e, 3, 0).tolist() == [0, 0, 0]
     with pytest.raises(oracle.OracleError):
         oracle.rows_typed("max", "i32", e, 3, 0)
+    # the empty product is 1 and the empty sum 0 for floating types too
+    for dt, npt in (("f32", np.float32), ("f16", np.float16)):
+        ef = np.zeros((3, 0), npt)
+        assert oracle.rows_typed("prod", dt, ef, 3, 0)[0].tolist() == [1.0, 1.0, 1.0]
+        assert oracle.rows_typed("sum", dt, ef, 3, 0)[0].tolist() == [0.0, 0.0, 0.0]
     r, _ = oracle.rows_typed("sum", "f16", np.full((1, 4), 0.5, np.float16), 1, 4, True,
                              np.array([1.0], np.float16))
     assert r.tolist() == [3.0]

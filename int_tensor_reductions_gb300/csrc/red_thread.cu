@@ -7,9 +7,10 @@
 // has a static size, like the page's local buffer), instantiated for
 // 1..RED_THREAD_MAX_LEN.  A CTA of 128 threads folds 128 consecutive rows;
 // their values (128 x len floats, contiguous) are staged through shared
-// memory with coalesced loads, at an odd row stride so that the threads'
-// row reads hit distinct banks, then each thread copies its row into
-// registers.
+// memory with coalesced loads (256-bit when the tile starts on a 32-byte
+// boundary, else one float per thread per load), at an odd row stride so
+// that the threads' row reads hit distinct banks, then each thread copies
+// its row into registers.
 #include "red_device.cuh"
 #include "red_internal.h"
 #include "red_prims.cuh"
@@ -19,6 +20,7 @@ namespace red {
 namespace {
 
 constexpr int TH_NT = 128;
+constexpr int TH_U = 4;  // 256-bit staging loads in flight per thread
 
 template <int OP, int N>
 __global__ void __launch_bounds__(TH_NT)
@@ -30,7 +32,30 @@ thread_rows_kernel(const float *__restrict__ x, int64_t rows, int accum, float *
     const int64_t r0 = (int64_t)blockIdx.x * TH_NT;
     const int nr = (int)((rows - r0) < TH_NT ? (rows - r0) : TH_NT);
     const float *src = x + r0 * N;
-    for (int g = threadIdx.x; g < nr * N; g += TH_NT) {
+    const int tot = nr * N;
+    int g0 = 0;  // elements below g0 are staged by the 256-bit loop
+    if ((((uintptr_t)src) & 31u) == 0) {
+        // 256-bit loads, TH_U in flight per thread before any shared store
+        const int nv = tot >> 3;
+        for (int c0 = threadIdx.x; c0 < nv; c0 += TH_U * TH_NT) {
+            float v[TH_U][8];
+#pragma unroll
+            for (int u = 0; u < TH_U; ++u)
+                if (c0 + u * TH_NT < nv)
+                    ld8(src + 8 * (c0 + u * TH_NT), v[u]);
+#pragma unroll
+            for (int u = 0; u < TH_U; ++u)
+                if (c0 + u * TH_NT < nv)
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int g = 8 * (c0 + u * TH_NT) + k;
+                        const int t = g / N, i = g - t * N;
+                        s_val[t * STRIDE + i] = v[u][k];
+                    }
+        }
+        g0 = nv << 3;
+    }
+    for (int g = g0 + threadIdx.x; g < tot; g += TH_NT) {
         const int t = g / N, i = g - t * N;
         s_val[t * STRIDE + i] = __ldg(src + g);
     }

@@ -36,10 +36,15 @@ def test_hand_worked_rounding_order():
         assert float(out[0]) == float(expected), name
 
 
+@pytest.mark.parametrize("shift", [0, 1])
 @pytest.mark.parametrize("length", list(range(1, 65)))
-def test_every_length_bit_exact(length):
+def test_every_length_bit_exact(length, shift):
+    """300 rows (two CTAs of 128 and a partial third); shift 0 stages the
+    32-byte aligned tiles with 256-bit loads, shift 1 (base 4 bytes past a
+    boundary) with the scalar loop."""
     rows = 300
-    x = synth.uniform((rows * length + 1,), -4.0, 4.0, length, device="cuda")[1:].view(rows, length)
+    x = synth.uniform((rows * length + 1,), -4.0, 4.0, length, device="cuda")[shift:shift + rows * length]
+    x = x.view(rows, length)
     dst = synth.uniform((rows,), -1.0, 1.0, 100 + length, device="cuda")
     xh, dh = to_host(x), to_host(dst)
     for accum in (False, True):

@@ -5,7 +5,9 @@
 //
 // The row length is a template parameter (the register array of the fold
 // has a static size, like the page's local buffer), instantiated for
-// 1..RED_THREAD_MAX_LEN.  A CTA of 128 threads folds 128 consecutive rows;
+// 1..RED_THREAD_MAX_LEN.  A CTA of 128 threads folds tiles of 128
+// consecutive rows (one tile per CTA, or a persistent grid looping over the
+// tiles when rows hold at most 8 floats);
 // their values (128 x len floats, contiguous) are staged through shared
 // memory with coalesced loads (256-bit when the tile starts on a 32-byte
 // boundary, else one float per thread per load), at an odd row stride so
@@ -29,59 +31,77 @@ thread_rows_kernel(const float *__restrict__ x, int64_t rows, int accum, float *
     constexpr int STRIDE = N | 1;  // odd row stride in shared memory
     __shared__ float s_val[TH_NT * STRIDE];
     pdl_enter();
-    const int64_t r0 = (int64_t)blockIdx.x * TH_NT;
-    const int nr = (int)((rows - r0) < TH_NT ? (rows - r0) : TH_NT);
-    const float *src = x + r0 * N;
-    const int tot = nr * N;
-    int g0 = 0;  // elements below g0 are staged by the 256-bit loop
-    if ((((uintptr_t)src) & 31u) == 0) {
-        // 256-bit loads, TH_U in flight per thread before any shared store
-        const int nv = tot >> 3;
-        for (int c0 = threadIdx.x; c0 < nv; c0 += TH_U * TH_NT) {
-            float v[TH_U][8];
+    const int64_t ntiles = (rows + TH_NT - 1) / TH_NT;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int64_t r0 = tile * TH_NT;
+        const int nr = (int)((rows - r0) < TH_NT ? (rows - r0) : TH_NT);
+        const float *src = x + r0 * N;
+        const int tot = nr * N;
+        int g0 = 0;  // elements below g0 are staged by the 256-bit loop
+        __syncthreads();  // the previous tile's reads of s_val are done
+        if ((((uintptr_t)src) & 31u) == 0) {
+            // 256-bit loads, TH_U in flight per thread before any shared store
+            const int nv = tot >> 3;
+            for (int c0 = threadIdx.x; c0 < nv; c0 += TH_U * TH_NT) {
+                float v[TH_U][8];
 #pragma unroll
-            for (int u = 0; u < TH_U; ++u)
-                if (c0 + u * TH_NT < nv)
-                    ld8(src + 8 * (c0 + u * TH_NT), v[u]);
+                for (int u = 0; u < TH_U; ++u)
+                    if (c0 + u * TH_NT < nv)
+                        ld8(src + 8 * (c0 + u * TH_NT), v[u]);
 #pragma unroll
-            for (int u = 0; u < TH_U; ++u)
-                if (c0 + u * TH_NT < nv)
+                for (int u = 0; u < TH_U; ++u)
+                    if (c0 + u * TH_NT < nv)
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int g = 8 * (c0 + u * TH_NT) + k;
-                        const int t = g / N, i = g - t * N;
-                        s_val[t * STRIDE + i] = v[u][k];
-                    }
+                        for (int k = 0; k < 8; ++k) {
+                            const int g = 8 * (c0 + u * TH_NT) + k;
+                            const int t = g / N, i = g - t * N;
+                            s_val[t * STRIDE + i] = v[u][k];
+                        }
+            }
+            g0 = nv << 3;
         }
-        g0 = nv << 3;
-    }
-    for (int g = g0 + threadIdx.x; g < tot; g += TH_NT) {
-        const int t = g / N, i = g - t * N;
-        s_val[t * STRIDE + i] = __ldg(src + g);
-    }
-    __syncthreads();
-    if (threadIdx.x >= nr)
-        return;
-    float a[N];
+        for (int g = g0 + threadIdx.x; g < tot; g += TH_NT) {
+            const int t = g / N, i = g - t * N;
+            s_val[t * STRIDE + i] = __ldg(src + g);
+        }
+        __syncthreads();
+        if (threadIdx.x < nr) {
+            float a[N];
 #pragma unroll
-    for (int i = 0; i < N; ++i)
-        a[i] = s_val[threadIdx.x * STRIDE + i];
-    const int64_t r = r0 + threadIdx.x;
-    const float old = accum ? out[r] : 0.0f;
-    float v;
-    if (OP == RED_SUM)
-        v = red_dev::thread_sum<N>(a, accum != 0, old);
-    else if (OP == RED_MAX)
-        v = red_dev::thread_max<N>(a, accum != 0, old);
-    else
-        v = red_dev::thread_min<N>(a, accum != 0, old);
-    out[r] = v;
+            for (int i = 0; i < N; ++i)
+                a[i] = s_val[threadIdx.x * STRIDE + i];
+            const int64_t r = r0 + threadIdx.x;
+            const float old = accum ? out[r] : 0.0f;
+            float v;
+            if (OP == RED_SUM)
+                v = red_dev::thread_sum<N>(a, accum != 0, old);
+            else if (OP == RED_MAX)
+                v = red_dev::thread_max<N>(a, accum != 0, old);
+            else
+                v = red_dev::thread_min<N>(a, accum != 0, old);
+            out[r] = v;
+        }
+    }
 }
 
 template <int OP, int N>
 int launch_n(const float *x, int64_t rows, int accum, float *out, cudaStream_t s)
 {
-    const int64_t ctas = (rows + TH_NT - 1) / TH_NT;
+    // Rows of at most 8 floats: a persistent grid of resident CTAs loops over
+    // the tiles of 128 rows (a tile is only 4 KB, and launching one CTA per
+    // tile costs more than the work); longer rows: one CTA per tile, whose
+    // staging overlaps other CTAs' folds (measured faster from 12 floats up).
+    DeviceInfo di;
+    const int st = device_info(&di);
+    if (st != RED_OK)
+        return st;
+    static std::atomic<int> occ_cache{0};
+    const int occ = cached_occupancy(occ_cache, (const void *)thread_rows_kernel<OP, N>, TH_NT);
+    if (occ <= 0)
+        return fail(RED_ECUDA, "red_rows_thread: kernel cannot be resident on this device");
+    int64_t ctas = (rows + TH_NT - 1) / TH_NT;
+    if (N <= 8 && ctas > (int64_t)di.sms * occ)
+        ctas = (int64_t)di.sms * occ;
     if (ctas > 0x7fffffffLL)
         return fail(RED_EINVAL, "red_rows_thread: too many rows");
     const cudaError_t e = launch_pdl(thread_rows_kernel<OP, N>, dim3((unsigned)ctas), dim3(TH_NT), s, x, rows, accum, out);

@@ -22,7 +22,11 @@ namespace red {
 namespace {
 
 constexpr int TH_NT = 128;
-constexpr int TH_U = 4;  // 256-bit staging loads in flight per thread
+// 256-bit staging loads in flight per thread: 4 (a 16 KB tile of rows of 32
+// in one batch), 8 for rows of 44 floats or more (measured: from 33 to 40
+// floats the extra registers cost more than the second batch)
+template <int N>
+__host__ __device__ constexpr int th_u() { return N >= 44 ? 8 : 4; }
 
 template <int OP, int N>
 __global__ void __launch_bounds__(TH_NT)
@@ -41,6 +45,7 @@ thread_rows_kernel(const float *__restrict__ x, int64_t rows, int accum, float *
         __syncthreads();  // the previous tile's reads of s_val are done
         if ((((uintptr_t)src) & 31u) == 0) {
             // 256-bit loads, TH_U in flight per thread before any shared store
+            constexpr int TH_U = th_u<N>();
             const int nv = tot >> 3;
             for (int c0 = threadIdx.x; c0 < nv; c0 += TH_U * TH_NT) {
                 float v[TH_U][8];

@@ -306,7 +306,9 @@ int red_release_workspace(void);
  * all threads), for counting launches around a timed region. */
 uint64_t red_launch_count(void);
 
-/* ABI version of this header: 1. */
+/* ABI version of this header: 2 (2: red_get_full_mode returns the setting,
+ * RED_MODE_AUTO included, because the automatic grid stage depends on the
+ * operator). */
 int red_version(void);
 
 #ifdef __cplusplus

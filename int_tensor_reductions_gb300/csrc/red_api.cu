@@ -380,6 +380,6 @@ int red_release_workspace(void)
 
 uint64_t red_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
-int red_version(void) { return 1; }
+int red_version(void) { return 2; }
 
 }  // extern "C"

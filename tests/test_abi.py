@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version(lib):
-    assert lib.red_version() == 1
+    assert lib.red_version() == 2
 
 
 def _err(lib):

@@ -28,7 +28,7 @@
  *          (dst[0,j] = prod_{i<R} src[i,j]) and "Constraints" (returns early
  *          when R == 0 or C == 0).
  *
- * Readings where the pages are silent (each one is also listed in the design doc):
+ * Readings where the pages are silent:
  *   - An empty dense input has no max / min: status -1 (error).  An empty
  *     ragged row folds nothing, so its max is -inf and its min +inf (with
  *     accum the old dst value survives); an empty sum is 0.

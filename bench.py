@@ -654,6 +654,30 @@ def small_cold_warm(w, stream, calls=20, reps=50):
     return res
 
 
+def graph_ms_per_call(fn, stream, calls=10, replays=5):
+    """Device time per call of ``calls`` back-to-back calls captured in one
+    CUDA graph and replayed ``replays`` times between two events, so that the
+    host's launch rate never leaves the GPU idle between short calls."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(calls):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(replays):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (replays * calls)
+    del g
+    return ms
+
+
 def supplementary(stream, dev, peak, reps=10):
     """The >= 1 GiB cases that grade the bandwidth bars of the row reductions
     and the column products (not part of the step): 262144 x 1024 fp32 rows
@@ -662,19 +686,10 @@ def supplementary(stream, dev, peak, reps=10):
     import torch
     import int_tensor_reductions_gb300 as itr
     from int_tensor_reductions_gb300 import synth
-    out = {"unit": "GB/s", "note": "1 GiB inputs, back-to-back calls, not part of the step"}
+    out = {"unit": "GB/s", "note": "1 GiB inputs, back-to-back calls replayed from a CUDA graph, not part of the step"}
 
     def timed(fn):
-        for _ in range(2):
-            fn()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(reps):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) / reps
+        return graph_ms_per_call(fn, stream, calls=reps)
 
     x = synth.normal((262144, 1024), 7, dev)
     o = torch.empty(262144, device=dev)
@@ -703,21 +718,13 @@ def column_ops(stream, dev, peak, reps=10):
     import torch
     import int_tensor_reductions_gb300 as itr
     from int_tensor_reductions_gb300 import synth
-    res = {"unit": "GB/s", "note": "back-to-back calls, inputs > L2 except the 8 MiB int16 case"}
+    res = {"unit": "GB/s", "note": "back-to-back calls replayed from a CUDA graph, inputs > L2 except the 8 MiB "
+                                   "int16 case (L2-resident between calls)"}
     for op, dtype, R, C in (("sum", "f32", 4096, 16384), ("prod", "f16", 4096, 16384), ("sum", "bf16", 8192, 16384),
                             ("max", "u32", 4096, 16384), ("prod", "i16", 64, 65536)):
         x = synth.col_input(op, dtype, (R, C), 11, dev)
         o = torch.empty(C, dtype=x.dtype, device=dev)
-        for _ in range(2):
-            itr.red_cols(op, x, o, dtype=dtype)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(reps):
-            itr.red_cols(op, x, o, dtype=dtype)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / reps
+        ms = graph_ms_per_call(lambda: itr.red_cols(op, x, o, dtype=dtype), stream, calls=reps)
         nbytes = x.numel() * x.element_size() + C * x.element_size()
         gbs = nbytes / (ms * 1e-3) / 1e9
         res[f"{op} {dtype} {R}x{C}"] = {"us": round(ms * 1e3, 1), "gbs": round(gbs, 1),
@@ -733,7 +740,7 @@ def typed_ops(stream, dev, peak, reps=10):
     import torch
     import int_tensor_reductions_gb300 as itr
     from int_tensor_reductions_gb300 import synth
-    res = {"unit": "GB/s", "note": "back-to-back calls, inputs > L2"}
+    res = {"unit": "GB/s", "note": "back-to-back calls replayed from a CUDA graph, inputs > L2"}
     cases = (("full", "sum", "i32", (1 << 28,)), ("full", "max", "f16", (1 << 29,)),
              ("rows", "sum", "i32", (65536, 1024)), ("rows", "max", "bf16", (65536, 2048)))
     for kind, op, dtype, shape in cases:
@@ -744,16 +751,7 @@ def typed_ops(stream, dev, peak, reps=10):
         else:
             o = torch.empty(shape[0], dtype=x.dtype, device=dev)
             fn = lambda: itr.red_rows_typed(op, x, out=o, dtype=dtype)  # noqa: E731
-        for _ in range(2):
-            fn()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(reps):
-            fn()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / reps
+        ms = graph_ms_per_call(fn, stream, calls=reps)
         nbytes = (x.numel() + o.numel()) * x.element_size()
         gbs = nbytes / (ms * 1e-3) / 1e9
         res[f"{kind} {op} {dtype} {'x'.join(map(str, shape))}"] = {"us": round(ms * 1e3, 1), "gbs": round(gbs, 1),

@@ -141,8 +141,15 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        return self.summarize(self.samples, self.window)
+
+    @classmethod
+    def summarize(cls, samples, window):
+        """Median SM clock, max clock and active throttle reasons of the
+        (time, nvidia-smi csv line) samples inside window (t0, t1), or of the
+        sample nearest its middle if none falls inside; None without samples."""
         rows = []
-        for t, line in self.samples:
+        for t, line in samples:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) != 8:
                 continue
@@ -152,10 +159,10 @@ class ClockSampler:
                 continue
         if not rows:
             return None
-        t0, t1 = self.window or (rows[0][0], rows[-1][0])
+        t0, t1 = window or (rows[0][0], rows[-1][0])
         inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05] or \
             [min(rows, key=lambda r: abs(r[0] - (t0 + t1) / 2))]
-        reasons = sorted({name for r in inside for name, v in zip(self.NAMES, r[3]) if v.lower() == "active"})
+        reasons = sorted({name for r in inside for name, v in zip(cls.NAMES, r[3]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
                 "reasons": reasons, "samples": len(inside)}
 

@@ -13,7 +13,13 @@ libred.so is missing or CUDA is unavailable, the calls raise.
     red_cols(op, x, out=None)                      column sum / max / min / prod
     red_full_typed / red_rows_typed                 full / per-row ops for every element type
     red_full_stats(x, out=None)                    sum, max, min, sum|x| in one read
+    red_rows_stats(x, out=None)                    the same per row, out: (rows, 4)
     red_rows_thread(op, x, accum=False, out=None)  one thread per row, the page's fold order
+    red_full_noalloc(op, x, out)                   red_full without any device allocation
+
+Every call takes an optional ``stream`` (default: the current stream of x's
+device) and returns ``out``.  Calls on one device must be ordered (one
+stream, or streams ordered by events): they share the library's workspace.
 """
 from ._binding import (  # noqa: F401
     RED_BF16, RED_EINVAL, RED_ECUDA, RED_ENOMEM, RED_F16, RED_F32, RED_I16, RED_I32, RED_KNOB_COLPROD_SPLITS,

@@ -51,6 +51,23 @@ __device__ __forceinline__ void prefetch_l2(const float *x, int64_t b, int64_t e
     prefetch_l2_bytes(x + b, x + e);
 }
 
+// Head and tail pieces of a row: L1-allocating loads (the interior blocks
+// bypass L1), so that a row's tail and the next row's head, which usually
+// share a 32-byte sector and are read by neighbouring lanes, meet in L1
+// (ragged rows of 8..40 floats: 76.3 -> 73.8 us).
+__device__ __forceinline__ float4 ld4p(const float *p)
+{
+    float4 v;
+    asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ float2 ld2p(const float *p)
+{
+    float2 v;
+    asm volatile("ld.global.nc.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+    return v;
+}
+
 template <int OP, int G, bool RAGGED>
 __global__ void __launch_bounds__(ROWS_NT, 3)
 rows_kernel(const float *__restrict__ x, const int64_t *__restrict__ off, int64_t rows, int64_t len,
@@ -138,17 +155,17 @@ rows_kernel(const float *__restrict__ x, const int64_t *__restrict__ off, int64_
                     if (h & 1)
                         hs = ld1(ph);
                     if (h & 2)
-                        h2 = ld2f(ph + (h & 1));
+                        h2 = ld2p(ph + (h & 1));
                     if (h & 4)
-                        h4 = ld4f(ph + (h & 3));
+                        h4 = ld4p(ph + (h & 3));
                 }
                 if (gl == G - 1) {
                     const int t = (int)(e - z);
                     const float *pt = x + z;
                     if (t & 4)
-                        t4 = ld4f(pt);
+                        t4 = ld4p(pt);
                     if (t & 2)
-                        t2 = ld2f(pt + (t & 4));
+                        t2 = ld2p(pt + (t & 4));
                     if (t & 1)
                         ts = ld1(pt + (t & 6));
                 }

@@ -218,6 +218,18 @@ int red_rows_ragged(int op, const float *x, const int64_t *offsets, int64_t rows
 int red_cols(int op, int dtype, const void *x, int64_t R, int64_t C, void *out, red_stream_t stream);
 
 /*
+ * red_cols_ld -- red_cols on the valid region of a larger row-major matrix:
+ * out[j] = op_{i=0}^{R-1} x[i*ld + j] for 0 <= j < C, row stride ld >= C
+ * (in elements).  This is [PTO] "Math Interpretation" with R = ValidRow and
+ * C = ValidCol of a row-major tile whose allocated width is ld; red_cols is
+ * the case ld == C.  Elements of x past column C of each row are never read.
+ * Arguments and errors as for red_cols; ld < C, or R * ld beyond the size
+ * limit: RED_EINVAL.
+ */
+int red_cols_ld(int op, int dtype, const void *x, int64_t R, int64_t C, int64_t ld, void *out,
+                red_stream_t stream);
+
+/*
  * red_full_typed / red_rows_typed -- red_full and red_rows for every element
  * type of red_cols (enum red_dtype) and every operator including RED_PROD:
  * out[0] = op over x[0..n); out[r] = op over row r = x[r*len .. r*len+len),

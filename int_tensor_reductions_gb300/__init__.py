@@ -10,7 +10,8 @@ libred.so is missing or CUDA is unavailable, the calls raise.
     red_rows(op, x, accum=False, out=None)         x: (rows, len) fp32
     red_rows_ragged(op, x, offsets, accum=False, out=None)
     red_colprod(x, out=None)                       x: (R, C) of any column element type
-    red_cols(op, x, out=None)                      column sum / max / min / prod
+    red_cols(op, x, out=None)                      column sum / max / min / prod (x may be a
+                                                   row-strided view: the C call red_cols_ld)
     red_full_typed / red_rows_typed                 full / per-row ops for every element type
     red_full_stats(x, out=None)                    sum, max, min, sum|x| in one read
     red_rows_stats(x, out=None)                    the same per row, out: (rows, 4)

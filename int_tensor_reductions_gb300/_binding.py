@@ -36,6 +36,7 @@ _SIGNATURES = {
     "red_rows_thread": ([_int, _vp, _i64, _int, _int, _vp, _vp], _int),
     "red_colprod": ([_int, _vp, _i64, _i64, _vp, _vp], _int),
     "red_cols": ([_int, _int, _vp, _i64, _i64, _vp, _vp], _int),
+    "red_cols_ld": ([_int, _int, _vp, _i64, _i64, _i64, _vp, _vp], _int),
     "red_full_typed": ([_int, _int, _vp, _i64, _vp, _vp], _int),
     "red_rows_typed": ([_int, _int, _vp, _i64, _i64, _int, _vp, _vp], _int),
     "red_set_full_mode": ([_int], _int),
@@ -242,15 +243,29 @@ def _col_dtype(x: torch.Tensor, dtype):
     return code
 
 
+def _row_strided(x: torch.Tensor, name: str = "x") -> int:
+    """Row stride (elements) of a 2-D CUDA view whose rows are contiguous."""
+    if not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if x.dim() != 2:
+        raise ValueError(f"{name} must be 2-D (R, C)")
+    R, C = x.shape
+    if R > 1 and C > 1 and x.stride(1) != 1:
+        raise ValueError(f"{name}'s rows must be contiguous (stride 1 along columns)")
+    ld = x.stride(0) if R > 1 else C
+    if ld < C:
+        raise ValueError(f"{name}'s row stride {ld} is smaller than its {C} columns")
+    return ld
+
+
 def red_cols(op, x: torch.Tensor, out: torch.Tensor | None = None, stream=None, dtype=None) -> torch.Tensor:
     """Column reduction out[j] = op_i x[i, j] (op "sum", "max", "min" or
     "prod") of a (R, C) matrix of float32, int32, float16, bfloat16, int16,
     uint16 or uint32; ``dtype`` ("u16", "u32", ...) reads x's storage as that
-    element type (same element size), e.g. int16 storage as uint16."""
-    if not x.is_cuda or not x.is_contiguous():
-        raise ValueError("x must be a contiguous CUDA tensor")
-    if x.dim() != 2:
-        raise ValueError("x must be 2-D (R, C)")
+    element type (same element size), e.g. int16 storage as uint16.  x may be
+    a view with contiguous rows and a larger row stride (e.g. ``big[:, :C]``):
+    the valid region of a wider tile."""
+    ld = _row_strided(x)
     code = _col_dtype(x, dtype)
     R, C = x.shape
     if out is None:
@@ -261,7 +276,7 @@ def red_cols(op, x: torch.Tensor, out: torch.Tensor | None = None, stream=None, 
     if out.numel() != C:
         raise ValueError("out must have C elements")
     with torch.cuda.device(x.device):
-        _check(lib().red_cols(_op(op), code, x.data_ptr(), R, C, out.data_ptr(), _stream(stream, x.device)))
+        _check(lib().red_cols_ld(_op(op), code, x.data_ptr(), R, C, ld, out.data_ptr(), _stream(stream, x.device)))
     return out
 
 
@@ -309,11 +324,9 @@ def red_rows_typed(op, x: torch.Tensor, accum: bool = False, out: torch.Tensor |
 
 def red_colprod(x: torch.Tensor, out: torch.Tensor | None = None, stream=None, dtype=None) -> torch.Tensor:
     """TCOLPROD: out[j] = prod_i x[i, j] for a (R, C) matrix of any element
-    type red_cols accepts (float32 rounds per step, integers wrap)."""
-    if not x.is_cuda or not x.is_contiguous():
-        raise ValueError("x must be a contiguous CUDA tensor")
-    if x.dim() != 2:
-        raise ValueError("x must be 2-D (R, C)")
+    type red_cols accepts (float32 rounds per step, integers wrap); x may have
+    a row stride larger than C (the valid region of a wider tile)."""
+    ld = _row_strided(x)
     code = _col_dtype(x, dtype)
     R, C = x.shape
     if out is None:
@@ -324,7 +337,7 @@ def red_colprod(x: torch.Tensor, out: torch.Tensor | None = None, stream=None, d
     if out.numel() != C:
         raise ValueError("out must have C elements")
     with torch.cuda.device(x.device):
-        _check(lib().red_colprod(code, x.data_ptr(), R, C, out.data_ptr(), _stream(stream, x.device)))
+        _check(lib().red_cols_ld(RED_PROD, code, x.data_ptr(), R, C, ld, out.data_ptr(), _stream(stream, x.device)))
     return out
 
 

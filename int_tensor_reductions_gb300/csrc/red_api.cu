@@ -249,22 +249,31 @@ int red_rows_ragged(int op, const float *x, const int64_t *offsets, int64_t rows
                          reinterpret_cast<cudaStream_t>(stream));
 }
 
-int red_cols(int op, int dtype, const void *x, int64_t R, int64_t C, void *out, red_stream_t stream)
+int red_cols_ld(int op, int dtype, const void *x, int64_t R, int64_t C, int64_t ld, void *out,
+                red_stream_t stream)
 {
     if (op < RED_SUM || op > RED_PROD)
         return fail(RED_EINVAL, "red_cols: unknown op %d", op);
     if (dtype < RED_F32 || dtype > RED_U32)
         return fail(RED_EINVAL, "red_cols: unknown dtype %d", dtype);
-    if (R < 0 || C < 0 || R > MAX_ELEMS || C > MAX_ELEMS || (C > 0 && R > MAX_ELEMS / C))
+    if (R < 0 || C < 0 || R > MAX_ELEMS || C > MAX_ELEMS)
         return fail(RED_EINVAL, "red_cols: R = %lld, C = %lld out of range", (long long)R, (long long)C);
+    if (ld < C || ld > MAX_ELEMS || (ld > 0 && R > MAX_ELEMS / ld))
+        return fail(RED_EINVAL, "red_cols: row stride ld = %lld must be >= C = %lld and R * ld in range",
+                    (long long)ld, (long long)C);
     if (R == 0 || C == 0)
-        return RED_OK;  // TCOLPROD returns early on an empty tile; dst untouched
+        return RED_OK;  // TCOLPROD returns early on an empty valid region; dst untouched
     const uintptr_t esz = (dtype == RED_F32 || dtype == RED_I32 || dtype == RED_U32) ? 4 : 2;
     if (!x || misaligned(x, esz))
         return fail(RED_EINVAL, "red_cols: x is NULL or not aligned to its element size");
     if (!out || misaligned(out, esz))
         return fail(RED_EINVAL, "red_cols: out is NULL or not aligned to its element size");
-    return launch_cols(op, dtype, x, R, C, out, reinterpret_cast<cudaStream_t>(stream));
+    return launch_cols(op, dtype, x, R, C, ld, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int red_cols(int op, int dtype, const void *x, int64_t R, int64_t C, void *out, red_stream_t stream)
+{
+    return red_cols_ld(op, dtype, x, R, C, C, out, stream);
 }
 
 namespace {

@@ -1,6 +1,7 @@
-// red_cols.cu -- column reductions dst[0,j] = op_{i<R} src[i,j] of a row-major
-// R x C matrix: TCOLPROD (pto-isa docs, "TCOLPROD", "Math Interpretation")
-// and its column siblings sum, max and min, for the element types of that
+// red_cols.cu -- column reductions dst[0,j] = op_{i<R} src[i,j] of the R x C
+// valid region of a row-major matrix with row stride ld >= C: TCOLPROD
+// (pto-isa docs, "TCOLPROD", "Math Interpretation") and its column siblings
+// sum, max and min, for the element types of that
 // page's A2A3 / A5 lists ("Constraints"): float, int32, half, bfloat16,
 // int16, uint16, uint32.  dst has src's element type.
 //
@@ -69,7 +70,7 @@ __device__ __forceinline__ void load_row(const typename Elem<DT>::T *p, typename
 
 template <int OP, int DT, int V>
 __global__ void __launch_bounds__(CP_NT, 2)
-cols_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t R, int64_t C, int64_t rows_per_split,
+cols_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t R, int64_t C, int64_t ld, int64_t rows_per_split,
             typename Elem<DT>::A *__restrict__ part, unsigned *__restrict__ tick, typename Elem<DT>::T *__restrict__ out)
 {
     pdl_enter();
@@ -97,7 +98,7 @@ cols_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t R, int64_t C, in
             A v[U][V];
 #pragma unroll
             for (int u = 0; u < U; ++u)
-                load_row<DT, V>(q + (i + u * CP_WY) * C, v[u]);
+                load_row<DT, V>(q + (i + u * CP_WY) * ld, v[u]);
 #pragma unroll
             for (int u = 0; u < U; ++u)
 #pragma unroll
@@ -106,7 +107,7 @@ cols_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t R, int64_t C, in
         }
         for (; i < i1; i += CP_WY) {
             A v[V];
-            load_row<DT, V>(q + i * C, v);
+            load_row<DT, V>(q + i * ld, v);
 #pragma unroll
             for (int k = 0; k < V; ++k)
                 p[k] = K::op(p[k], v[k]);
@@ -161,7 +162,7 @@ cols_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t R, int64_t C, in
 }
 
 template <int OP, int DT, int V>
-int launch_cols(const void *xv, int64_t R, int64_t C, void *outv, cudaStream_t s, const DeviceInfo &di)
+int launch_cols(const void *xv, int64_t R, int64_t C, int64_t ld, void *outv, cudaStream_t s, const DeviceInfo &di)
 {
     using E = Elem<DT>;
     using T = typename E::T;
@@ -221,7 +222,7 @@ int launch_cols(const void *xv, int64_t R, int64_t C, void *outv, cudaStream_t s
             return st;
     }
     const dim3 grid((unsigned)tiles, (unsigned)splits);
-    const cudaError_t e = launch_pdl(cols_kernel<OP, DT, V>, grid, dim3(CP_NT), s, static_cast<const T *>(xv), R, C,
+    const cudaError_t e = launch_pdl(cols_kernel<OP, DT, V>, grid, dim3(CP_NT), s, static_cast<const T *>(xv), R, C, ld,
                                      rps, static_cast<A *>(ws.part), ws.tick, static_cast<T *>(outv));
     count_launches(1);
     return cuda_fail(e != cudaSuccess ? e : cudaGetLastError(), "red_cols launch");
@@ -230,45 +231,46 @@ int launch_cols(const void *xv, int64_t R, int64_t C, void *outv, cudaStream_t s
 // Vector width by alignment: 32-byte rows and base -> 256-bit loads,
 // 16-byte -> 128-bit, otherwise one element per lane.
 template <int OP, int DT>
-int launch_cols_dt(const void *x, int64_t R, int64_t C, void *out, cudaStream_t s, const DeviceInfo &di)
+int launch_cols_dt(const void *x, int64_t R, int64_t C, int64_t ld, void *out, cudaStream_t s, const DeviceInfo &di)
 {
     constexpr int SZ = (int)sizeof(typename Elem<DT>::T);
     const uintptr_t a = (uintptr_t)x;
-    const int64_t row_bytes = C * SZ;
+    const int64_t row_bytes = ld * SZ;  // row stride: every row start must keep the alignment
     if (row_bytes % 32 == 0 && a % 32 == 0)
-        return launch_cols<OP, DT, 32 / SZ>(x, R, C, out, s, di);
+        return launch_cols<OP, DT, 32 / SZ>(x, R, C, ld, out, s, di);
     if (row_bytes % 16 == 0 && a % 16 == 0)
-        return launch_cols<OP, DT, 16 / SZ>(x, R, C, out, s, di);
-    return launch_cols<OP, DT, 1>(x, R, C, out, s, di);
+        return launch_cols<OP, DT, 16 / SZ>(x, R, C, ld, out, s, di);
+    return launch_cols<OP, DT, 1>(x, R, C, ld, out, s, di);
 }
 
 template <int OP>
-int launch_cols_op(int dtype, const void *x, int64_t R, int64_t C, void *out, cudaStream_t s, const DeviceInfo &di)
+int launch_cols_op(int dtype, const void *x, int64_t R, int64_t C, int64_t ld, void *out, cudaStream_t s,
+                   const DeviceInfo &di)
 {
     switch (dtype) {
-    case RED_F32: return launch_cols_dt<OP, RED_F32>(x, R, C, out, s, di);
-    case RED_I32: return launch_cols_dt<OP, RED_I32>(x, R, C, out, s, di);
-    case RED_F16: return launch_cols_dt<OP, RED_F16>(x, R, C, out, s, di);
-    case RED_BF16: return launch_cols_dt<OP, RED_BF16>(x, R, C, out, s, di);
-    case RED_I16: return launch_cols_dt<OP, RED_I16>(x, R, C, out, s, di);
-    case RED_U16: return launch_cols_dt<OP, RED_U16>(x, R, C, out, s, di);
-    default: return launch_cols_dt<OP, RED_U32>(x, R, C, out, s, di);
+    case RED_F32: return launch_cols_dt<OP, RED_F32>(x, R, C, ld, out, s, di);
+    case RED_I32: return launch_cols_dt<OP, RED_I32>(x, R, C, ld, out, s, di);
+    case RED_F16: return launch_cols_dt<OP, RED_F16>(x, R, C, ld, out, s, di);
+    case RED_BF16: return launch_cols_dt<OP, RED_BF16>(x, R, C, ld, out, s, di);
+    case RED_I16: return launch_cols_dt<OP, RED_I16>(x, R, C, ld, out, s, di);
+    case RED_U16: return launch_cols_dt<OP, RED_U16>(x, R, C, ld, out, s, di);
+    default: return launch_cols_dt<OP, RED_U32>(x, R, C, ld, out, s, di);
     }
 }
 
 }  // namespace
 
-int launch_cols(int op, int dtype, const void *x, int64_t R, int64_t C, void *out, cudaStream_t s)
+int launch_cols(int op, int dtype, const void *x, int64_t R, int64_t C, int64_t ld, void *out, cudaStream_t s)
 {
     DeviceInfo di;
     const int st = device_info(&di);
     if (st != RED_OK)
         return st;
     switch (op) {
-    case RED_SUM: return launch_cols_op<RED_SUM>(dtype, x, R, C, out, s, di);
-    case RED_MAX: return launch_cols_op<RED_MAX>(dtype, x, R, C, out, s, di);
-    case RED_MIN: return launch_cols_op<RED_MIN>(dtype, x, R, C, out, s, di);
-    default: return launch_cols_op<RED_PROD>(dtype, x, R, C, out, s, di);
+    case RED_SUM: return launch_cols_op<RED_SUM>(dtype, x, R, C, ld, out, s, di);
+    case RED_MAX: return launch_cols_op<RED_MAX>(dtype, x, R, C, ld, out, s, di);
+    case RED_MIN: return launch_cols_op<RED_MIN>(dtype, x, R, C, ld, out, s, di);
+    default: return launch_cols_op<RED_PROD>(dtype, x, R, C, ld, out, s, di);
     }
 }
 

@@ -84,6 +84,16 @@ def test_colprod_rejects_and_returns_early(lib):
     assert lib.red_colprod(RED_F32, None, 4, 0, None, None) == RED_OK
 
 
+def test_cols_ld_rejects_and_returns_early(lib):
+    """Row stride of the valid region (pto-isa docs, "TCOLPROD", "Math
+    Interpretation": R x C = ValidRow x ValidCol of a wider row-major tile)."""
+    from int_tensor_reductions_gb300 import RED_EINVAL, RED_F32, RED_OK
+    assert lib.red_cols_ld(0, RED_F32, 0x1000, 4, 8, 7, 0x2000, None) == RED_EINVAL   # ld < C
+    assert lib.red_cols_ld(0, RED_F32, 0x1000, 1 << 40, 8, 1 << 20, 0x2000, None) == RED_EINVAL  # R * ld too big
+    assert lib.red_cols_ld(3, RED_F32, None, 0, 8, 16, None, None) == RED_OK          # empty: early return
+    assert lib.red_cols_ld(3, RED_F32, None, 4, 0, 16, None, None) == RED_OK
+
+
 def test_knobs_and_modes(lib):
     import int_tensor_reductions_gb300 as itr
     assert lib.red_set_full_mode(9) == itr.RED_EINVAL

@@ -57,7 +57,7 @@ def check_cols(op, dtype, x: torch.Tensor, what, cols=None):
     R, C = x.shape
     out = itr.red_cols(op, x, dtype=dtype)
     got = _decode(out, dtype)
-    xh = x.cpu()
+    xh = x.cpu().contiguous()  # x may be a row-strided view
     if cols is not None:
         xh = xh[:, cols].contiguous()
         got = got[cols]
@@ -154,3 +154,23 @@ def test_early_return_every_type():
         out = torch.full((5,), 3, dtype=st, device="cuda")
         itr.red_cols("max", torch.empty((0, 5), dtype=st, device="cuda"), out, dtype=dtype)
         assert (out.cpu() == 3).all(), dtype
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("R,C,ld", [(37, 100, 104), (500, 1040, 1056), (64, 4096, 5000), (3, 1, 9), (1, 17, 40)])
+def test_valid_region_of_a_wider_matrix(R, C, ld, dtype):
+    """TCOLPROD over the valid region R x C of a row-major matrix whose rows
+    are ld elements apart (pto-isa docs, "TCOLPROD", "Math Interpretation":
+    R = ValidRow, C = ValidCol).  The columns past C hold values that would
+    change every result if they were read (NaN for floats; for integers the
+    type's extreme values)."""
+    for op in OPS:
+        full = synth.col_input(op, dtype, (R, ld), R * 3 + C, device="cuda")
+        pad = full[:, C:]
+        if full.is_floating_point():
+            pad.fill_(float("nan"))
+        else:
+            pad.fill_(-1 if dtype in ("u16", "u32") else torch.iinfo(full.dtype).min)
+        check_cols(op, dtype, full[:, :C], f"{op} {dtype} {R}x{C} ld={ld}")
+    p = itr.red_colprod(synth.col_input("prod", dtype, (R, ld), 5, device="cuda")[:, :C], dtype=dtype)
+    assert p.numel() == C

@@ -154,7 +154,9 @@ int red_rows_stats(const float *x, int64_t rows, int64_t len, float *out, red_st
  *   accum  0: overwrite out; non-zero: fold the old out[r] in.
  *   out    device pointer to rows floats (read first when accum != 0).
  * len == 0: RED_SUM writes zeros (accum: leaves out unchanged); RED_MAX /
- * RED_MIN return RED_EINVAL.  rows == 0 does nothing.
+ * RED_MIN return RED_EINVAL.  rows == 0 does nothing.  Rows of at most
+ * RED_THREAD_MAX_LEN floats are reduced as red_rows_thread does (one thread
+ * per row, the thread-scope fold), which is the faster layout for them.
  */
 int red_rows(int op, const float *x, int64_t rows, int64_t len, int accum, float *out,
              red_stream_t stream);

@@ -67,6 +67,9 @@ def parse_args():
                          "colprod4b); for profiling: the line is then not the benchmark's metric")
     ap.add_argument("--scale", type=float, default=1.0,
                     help="fraction of every workload's size (rows / elements); for profiling")
+    ap.add_argument("--sweep", action="store_true",
+                    help="print per-call GB/s of every entry point over a range of shapes (one JSON line "
+                         "per case, CUDA-graph replays), then exit; not the benchmark's metric")
     ap.add_argument("--case", default="", choices=[""] + sorted(CASES),
                     help="run one extra library case (not the step) --steps times after --warmup, for profiling")
     return ap.parse_args()
@@ -839,8 +842,59 @@ def cpu_baseline(w, min_seconds=10.0):
             "seconds": round(secs, 2), "host_cpus": os.cpu_count()}
 
 
+def run_sweep(args):
+    """Per-call device GB/s (algorithmic bytes over graph-replayed time) of
+    the entry points across shapes, from L2-sized to several GiB."""
+    import torch
+    import int_tensor_reductions_gb300 as itr
+    from int_tensor_reductions_gb300 import _build, synth
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _build.build_lib()
+    stream = torch.cuda.current_stream(dev)
+
+    def emit(kind, shape, fn, nbytes):
+        ms = graph_ms_per_call(fn, stream, calls=5, replays=4)
+        print(json.dumps({"sweep": kind, "shape": shape, "us": round(ms * 1e3, 2),
+                          "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}), flush=True)
+
+    for n in (1 << 16, 1 << 20, 1 << 24, 1 << 28, 1 << 30, (1 << 31) + 3):
+        x = synth.uniform((n,), -1.0, 1.0, 1, dev)
+        o = torch.empty(1, device=dev)
+        for op in ("sum", "max"):
+            emit(f"red_full {op}", [n], lambda: itr.red_full(op, x, o), 4 * n + 4)
+        del x, o
+        torch.cuda.empty_cache()
+    for rows, length in ((1 << 23, 16), (1 << 21, 64), (1 << 19, 256), (1 << 18, 1024), (1 << 12, 1 << 16),
+                         (16, 1 << 24), (3, 1 << 28)):
+        x = synth.uniform((rows, length), -1.0, 1.0, 2, dev)
+        o = torch.empty(rows, device=dev)
+        emit("red_rows sum", [rows, length], lambda: itr.red_rows("sum", x, out=o), 4 * rows * length + 4 * rows)
+        del x, o
+        torch.cuda.empty_cache()
+    for mean in (4, 24, 100, 1000):
+        rows = (1 << 27) // mean
+        off = synth.ragged_offsets(rows, max(1, mean // 2), mean + mean // 2, 3, dev)
+        nnz = int(off[-1].item())
+        x = synth.uniform((nnz,), -1.0, 1.0, 4, dev)
+        o = torch.empty(rows, device=dev)
+        emit("red_rows_ragged sum", [rows, f"lengths {max(1, mean // 2)}..{mean + mean // 2}"],
+             lambda: itr.red_rows_ragged("sum", x, off, out=o), 4 * nnz + 8 * (rows + 1) + 4 * rows)
+        del x, o, off
+        torch.cuda.empty_cache()
+    for R, C in ((1 << 20, 64), (1 << 16, 1024), (4096, 16384), (64, 1 << 20), (16384, 16384)):
+        x = synth.uniform((R, C), -1.0, 1.0, 5, dev)
+        o = torch.empty(C, device=dev)
+        emit("red_cols sum", [R, C], lambda: itr.red_cols("sum", x, o), 4 * R * C + 4 * C)
+        del x, o
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.sweep:
+        return run_sweep(args)
     if args.case:
         return run_case(args)
     if args.impl == "reference":

@@ -294,8 +294,10 @@ int launch_rows_split(int op, const float *x, int64_t rows, int64_t len, int acc
     const int occ = ctas_per_sm(op, STAGE_LAST_BLOCK);
     if (occ <= 0)
         return fail(RED_ECUDA, "red_rows: kernel cannot be resident on this device");
+    // rows * splits CTAs in one wave of resident CTAs (rounding the split
+    // count up would leave a few CTAs to run alone after the wave)
     const int64_t target = (int64_t)di.sms * occ;
-    int64_t splits = ceil_div(target, rows);
+    int64_t splits = target / rows;
     const int64_t need = ceil_div(len / 8 + 1, (int64_t)FULL_NT * FULL_U);
     if (splits > need)
         splits = need;

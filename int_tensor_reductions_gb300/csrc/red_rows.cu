@@ -272,9 +272,17 @@ int launch_rows(int op, const float *x, int64_t rows, int64_t len, int accum, fl
     // such length (rows of 32: 7.0 vs 5.6 TB/s; of 8: 5.0 vs 4.2).
     if (knob(RED_KNOB_ROWS_GROUP) == 0 && len <= RED_THREAD_MAX_LEN)
         return launch_rows_thread(op, x, rows, (int)len, accum, out, s);
-    // Few long rows cannot fill the GPU with one group per row: split each
-    // row over several CTAs.
-    if (knob(RED_KNOB_ROWS_GROUP) == 0 && len >= 8192 && rows < (int64_t)di.sms * 16)
+    // Long rows go to the segmented kernel (CTAs per row) when there are too
+    // few rows to fill the GPU with one lane group per row, and for rows of
+    // 32768 floats or more when they outnumber the row kernel's warps (24 per
+    // SM): a warp per row would then finish with a partial second pass,
+    // while CTAs per 128+ KB row balance over many waves (4096 x 65536: 7.35
+    // vs 6.43 TB/s).  With fewer such rows every row has its own warp and
+    // the row kernel stays (2500 x 40000: 6.64 vs 6.02); rows of 8K-16K
+    // floats stay too (the CTA stage costs more than it gains).  The
+    // segmented grid holds one row per gridDim.y index, at most 65535.
+    if (knob(RED_KNOB_ROWS_GROUP) == 0 && len >= 8192 &&
+        (rows < (int64_t)di.sms * 16 || (len >= 32768 && rows > (int64_t)di.sms * 24 && rows <= 65535)))
         return launch_rows_split(op, x, rows, len, accum, out, s, di);
     const int g = knob(RED_KNOB_ROWS_GROUP) ? knob(RED_KNOB_ROWS_GROUP) : auto_group(len);
     return launch_op<false>(op, g, x, nullptr, rows, len, 0, accum, out, s, di.sms);

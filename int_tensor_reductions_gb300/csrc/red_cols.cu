@@ -11,15 +11,17 @@
 // (done in 32-bit unsigned arithmetic, then truncated for the 16-bit types);
 // max / min compare values (signed or unsigned as the type is).
 //
-// Layout of the work: a CTA owns a tile of 32*V adjacent columns and 16
-// warps.  Lane l of every warp owns V adjacent columns of the tile and keeps
-// V running accumulators (per-thread column accumulators); warp w walks rows
-// i0+w, i0+w+16, ... of the CTA's row slab, so each warp reads 32 bytes per
-// lane of a row per load (coalesced, row-major order kept).  The 16 warp
-// results meet in shared memory (fixed order).  gridDim.y CTAs split the
-// rows; with more than one, the CTA partials go to the workspace and the CTA
-// that arrives last for its column tile folds them (in split order) into
-// dst.  No CTA ever waits for another.
+// Layout of the work: a CTA of 16 warps owns a tile of lpr*V adjacent
+// columns, lpr lanes per row (32, or the power of two that covers a narrower
+// matrix, whose warps then take 32/lpr consecutive rows per step, so no lane
+// idles).  Each lane owns V adjacent columns and keeps V running
+// accumulators (per-thread column accumulators); the lane groups of warp w
+// walk rows i0 + w*32/lpr, ... in steps of 16*32/lpr rows, each lane reading
+// 32 bytes of a row per load (coalesced, row-major order kept).  The row
+// groups of a warp meet in a butterfly, the 16 warps in shared memory (fixed
+// order).  gridDim.y CTAs split the rows; with more than one, the CTA
+// partials go to the workspace and the CTA that arrives last for its column
+// tile folds them (in split order) into dst.  No CTA ever waits for another.
 #include "red_internal.h"
 #include "red_prims.cuh"
 #include "red_types.cuh"
@@ -71,7 +73,8 @@ __device__ __forceinline__ void load_row(const typename Elem<DT>::T *p, typename
 template <int OP, int DT, int V>
 __global__ void __launch_bounds__(CP_NT, 2)
 cols_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t R, int64_t C, int64_t ld, int64_t rows_per_split,
-            typename Elem<DT>::A *__restrict__ part, unsigned *__restrict__ tick, typename Elem<DT>::T *__restrict__ out)
+            int lpr, typename Elem<DT>::A *__restrict__ part, unsigned *__restrict__ tick,
+            typename Elem<DT>::T *__restrict__ out)
 {
     pdl_enter();
     using E = Elem<DT>;
@@ -81,11 +84,17 @@ cols_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t R, int64_t C, in
     __shared__ A s_p[CP_WY][32 * V];
     __shared__ int s_last;
 
+    // lpr lanes (a power of two) cover a row of the tile; the warp's 32 / lpr
+    // lane groups take consecutive rows, so narrow matrices keep every lane busy
     const int lane = threadIdx.x & 31, wy = threadIdx.x >> 5;
-    const int64_t col = ((int64_t)blockIdx.x * 32 + lane) * V;
+    const int rpw = 32 / lpr;           // rows per warp step
+    const int cl = lane & (lpr - 1);    // lane within its row group
+    const int sub = lane / lpr;         // row group within the warp
+    const int64_t col = ((int64_t)blockIdx.x * lpr + cl) * V;
     const bool live = col < C;  // V > 1 only when C % V == 0
     const int64_t i0 = (int64_t)blockIdx.y * rows_per_split;
     const int64_t i1 = (i0 + rows_per_split < R) ? i0 + rows_per_split : R;
+    const int64_t step = (int64_t)CP_WY * rpw;
 
     A p[V];
 #pragma unroll
@@ -93,19 +102,19 @@ cols_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t R, int64_t C, in
         p[k] = K::identity();
     if (live) {
         const typename E::T *q = x + col;
-        int64_t i = i0 + wy;
-        for (; i + (U - 1) * CP_WY < i1; i += U * CP_WY) {
+        int64_t i = i0 + (int64_t)wy * rpw + sub;
+        for (; i + (U - 1) * step < i1; i += U * step) {
             A v[U][V];
 #pragma unroll
             for (int u = 0; u < U; ++u)
-                load_row<DT, V>(q + (i + u * CP_WY) * ld, v[u]);
+                load_row<DT, V>(q + (i + u * step) * ld, v[u]);
 #pragma unroll
             for (int u = 0; u < U; ++u)
 #pragma unroll
                 for (int k = 0; k < V; ++k)
                     p[k] = K::op(p[k], v[u][k]);
         }
-        for (; i < i1; i += CP_WY) {
+        for (; i < i1; i += step) {
             A v[V];
             load_row<DT, V>(q + i * ld, v);
 #pragma unroll
@@ -113,26 +122,33 @@ cols_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t R, int64_t C, in
                 p[k] = K::op(p[k], v[k]);
         }
     }
+    // the row groups of the warp meet (butterfly over the group bits)
+    for (int o = lpr; o < 32; o <<= 1)
 #pragma unroll
-    for (int k = 0; k < V; ++k)
-        s_p[wy][lane * V + k] = p[k];
+        for (int k = 0; k < V; ++k)
+            p[k] = K::op(p[k], __shfl_xor_sync(0xffffffffu, p[k], o));
+    if (sub == 0)
+#pragma unroll
+        for (int k = 0; k < V; ++k)
+            s_p[wy][cl * V + k] = p[k];
     __syncthreads();
-    if (wy == 0) {
+    if (wy == 0 && sub == 0) {
 #pragma unroll
         for (int w = 1; w < CP_WY; ++w)
 #pragma unroll
             for (int k = 0; k < V; ++k)
-                p[k] = K::op(p[k], s_p[w][lane * V + k]);
+                p[k] = K::op(p[k], s_p[w][cl * V + k]);
     }
+    const bool writer = wy == 0 && sub == 0 && live;
 
     if (gridDim.y == 1) {
-        if (wy == 0 && live)
+        if (writer)
 #pragma unroll
             for (int k = 0; k < V; ++k)
                 out[col + k] = E::narrow(p[k]);
         return;
     }
-    if (wy == 0 && live)
+    if (writer)
 #pragma unroll
         for (int k = 0; k < V; ++k)
             part[(int64_t)blockIdx.y * C + col + k] = p[k];
@@ -144,7 +160,7 @@ cols_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t R, int64_t C, in
     if (!s_last)
         return;
     __threadfence();
-    if (wy == 0 && live) {
+    if (writer) {
         A q[V];
 #pragma unroll
         for (int k = 0; k < V; ++k)
@@ -172,7 +188,13 @@ int launch_cols(const void *xv, int64_t R, int64_t C, int64_t ld, void *outv, cu
     if (occ <= 0)
         return fail(RED_ECUDA, "red_cols: kernel cannot be resident on this device");
     constexpr int U = sizeof(T) == 4 ? 4 : 2;
-    const int64_t tile_cols = 32 * V;
+    // lanes per row: enough V-wide chunks for C columns, a power of two <= 32
+    const int64_t chunks = (C + V - 1) / V;
+    int lpr = 1;
+    while (lpr < 32 && lpr < chunks)
+        lpr *= 2;
+    const int rpw = 32 / lpr;
+    const int64_t tile_cols = (int64_t)lpr * V;
     const int64_t tiles = (C + tile_cols - 1) / tile_cols;
     if (tiles > 0x7fffffffLL)
         return fail(RED_EINVAL, "red_cols: C too large");
@@ -183,7 +205,7 @@ int launch_cols(const void *xv, int64_t R, int64_t C, int64_t ld, void *outv, cu
     int64_t splits = knob(RED_KNOB_COLPROD_SPLITS);
     if (splits <= 0) {
         const int64_t slots = (int64_t)di.sms * occ;
-        int64_t smax = R / (CP_WY * U);
+        int64_t smax = R / ((int64_t)CP_WY * U * rpw);
         if (smax > 4096)
             smax = 4096;
         if (smax < 1)
@@ -223,7 +245,7 @@ int launch_cols(const void *xv, int64_t R, int64_t C, int64_t ld, void *outv, cu
     }
     const dim3 grid((unsigned)tiles, (unsigned)splits);
     const cudaError_t e = launch_pdl(cols_kernel<OP, DT, V>, grid, dim3(CP_NT), s, static_cast<const T *>(xv), R, C, ld,
-                                     rps, static_cast<A *>(ws.part), ws.tick, static_cast<T *>(outv));
+                                     rps, lpr, static_cast<A *>(ws.part), ws.tick, static_cast<T *>(outv));
     count_launches(1);
     return cuda_fail(e != cudaSuccess ? e : cudaGetLastError(), "red_cols launch");
 }
@@ -235,10 +257,13 @@ int launch_cols_dt(const void *x, int64_t R, int64_t C, int64_t ld, void *out, c
 {
     constexpr int SZ = (int)sizeof(typename Elem<DT>::T);
     const uintptr_t a = (uintptr_t)x;
-    const int64_t row_bytes = ld * SZ;  // row stride: every row start must keep the alignment
-    if (row_bytes % 32 == 0 && a % 32 == 0)
+    // Every row start keeps the alignment (ld), and C is a whole number of
+    // vectors, so a lane's V columns never pass column C (neither the reads
+    // of a row nor the writes to out).
+    const int64_t row_bytes = ld * SZ, valid_bytes = C * SZ;
+    if (row_bytes % 32 == 0 && valid_bytes % 32 == 0 && a % 32 == 0)
         return launch_cols<OP, DT, 32 / SZ>(x, R, C, ld, out, s, di);
-    if (row_bytes % 16 == 0 && a % 16 == 0)
+    if (row_bytes % 16 == 0 && valid_bytes % 16 == 0 && a % 16 == 0)
         return launch_cols<OP, DT, 16 / SZ>(x, R, C, ld, out, s, di);
     return launch_cols<OP, DT, 1>(x, R, C, ld, out, s, di);
 }

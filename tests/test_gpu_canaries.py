@@ -117,3 +117,16 @@ def test_cols_and_typed(dtype, splits):
                 _intact(buf, 1, 0, f"red_full_typed {op} {dtype} {R}x{C}")
     finally:
         itr.red_set_knob(itr.RED_KNOB_COLPROD_SPLITS, 0)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "i32"])
+def test_cols_valid_region_of_wider_rows(dtype):
+    """Column reductions of the R x C valid region of rows ld > C apart:
+    nothing is written past out[C - 1], whatever vector width ld allows."""
+    for R, C, ld in ((37, 100, 104), (9, 12, 16), (64, 1000, 1024), (5, 3, 64), (300, 24, 40)):
+        for op in ("sum", "prod"):
+            full = synth.col_input(op, dtype, (R, ld), R + C, device="cuda")
+            buf, out = _guarded(C, full.dtype)
+            itr.red_cols(op, full[:, :C], out, dtype=dtype)
+            _intact(buf, C, 0, f"red_cols {op} {dtype} {R}x{C} ld={ld}")
+

@@ -21,7 +21,8 @@
 // groups of a warp meet in a butterfly, the 16 warps in shared memory (fixed
 // order).  gridDim.y CTAs split the rows; with more than one, the CTA
 // partials go to the workspace and the CTA that arrives last for its column
-// tile folds them (in split order) into dst.  No CTA ever waits for another.
+// tile folds them, with all its lanes in a fixed order, into dst.  No CTA
+// ever waits for another.
 #include "red_internal.h"
 #include "red_prims.cuh"
 #include "red_types.cuh"
@@ -160,15 +161,35 @@ cols_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t R, int64_t C, in
     if (!s_last)
         return;
     __threadfence();
-    if (writer) {
-        A q[V];
+    // The last CTA folds the gridDim.y partials of its tile with all of its
+    // lanes: row group g of warp w takes splits w*rpw+g, w*rpw+g + 16*rpw, ...
+    // (a fixed assignment), then the groups meet in a butterfly and the warps
+    // in shared memory, in warp order.
+    A q[V];
 #pragma unroll
-        for (int k = 0; k < V; ++k)
-            q[k] = K::identity();
-        for (unsigned sp = 0; sp < gridDim.y; ++sp)
+    for (int k = 0; k < V; ++k)
+        q[k] = K::identity();
+    if (live)
+        for (int64_t sp = (int64_t)wy * rpw + sub; sp < (int64_t)gridDim.y; sp += step)
 #pragma unroll
             for (int k = 0; k < V; ++k)
-                q[k] = K::op(q[k], ldcg_a<A>(part + (int64_t)sp * C + col + k));
+                q[k] = K::op(q[k], ldcg_a<A>(part + sp * C + col + k));
+    for (int o = lpr; o < 32; o <<= 1)
+#pragma unroll
+        for (int k = 0; k < V; ++k)
+            q[k] = K::op(q[k], __shfl_xor_sync(0xffffffffu, q[k], o));
+    __syncthreads();  // every read of s_p above is done
+    if (sub == 0)
+#pragma unroll
+        for (int k = 0; k < V; ++k)
+            s_p[wy][cl * V + k] = q[k];
+    __syncthreads();
+    if (writer) {
+#pragma unroll
+        for (int w = 1; w < CP_WY; ++w)
+#pragma unroll
+            for (int k = 0; k < V; ++k)
+                q[k] = K::op(q[k], s_p[w][cl * V + k]);
 #pragma unroll
         for (int k = 0; k < V; ++k)
             out[col + k] = E::narrow(q[k]);

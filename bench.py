@@ -888,6 +888,36 @@ def run_sweep(args):
         emit("red_cols sum", [R, C], lambda: itr.red_cols("sum", x, o), 4 * R * C + 4 * C)
         del x, o
         torch.cuda.empty_cache()
+    for dtype, R, C in (("f16", 1 << 21, 64), ("f16", 8192, 16384), ("i16", 64, 1 << 21), ("bf16", 1 << 17, 1024)):
+        x = synth.col_input("sum", dtype, (R, C), 6, dev)
+        o = torch.empty(C, dtype=x.dtype, device=dev)
+        emit(f"red_cols sum {dtype}", [R, C], lambda: itr.red_cols("sum", x, o, dtype=dtype),
+             x.element_size() * (R * C + C))
+        del x, o
+        torch.cuda.empty_cache()
+    for dtype, shape in (("f16", (1 << 28,)), ("i32", (1 << 27,)), ("bf16", (1 << 22, 64)), ("i32", (1 << 23, 16)),
+                         ("f16", (4096, 1 << 16)), ("u16", (1 << 24, 8))):
+        x = synth.col_input("max", dtype, shape, 7, dev)
+        if len(shape) == 1:
+            o = torch.empty(1, dtype=x.dtype, device=dev)
+            emit(f"red_full_typed max {dtype}", list(shape), lambda: itr.red_full_typed("max", x, o, dtype=dtype),
+                 x.element_size() * (x.numel() + 1))
+        else:
+            o = torch.empty(shape[0], dtype=x.dtype, device=dev)
+            emit(f"red_rows_typed max {dtype}", list(shape), lambda: itr.red_rows_typed("max", x, out=o, dtype=dtype),
+                 x.element_size() * (x.numel() + shape[0]))
+        del x, o
+        torch.cuda.empty_cache()
+    x = synth.uniform((1 << 28,), -1.0, 1.0, 8, dev)
+    o = torch.empty(4, device=dev)
+    emit("red_full_stats", [1 << 28], lambda: itr.red_full_stats(x, o), 4 * (1 << 28) + 16)
+    del x, o
+    for rows, length in ((1 << 23, 16), (1 << 21, 64), (1 << 17, 1024)):
+        x = synth.uniform((rows, length), -1.0, 1.0, 9, dev)
+        o = torch.empty((rows, 4), device=dev)
+        emit("red_rows_stats", [rows, length], lambda: itr.red_rows_stats(x, o), 4 * rows * length + 16 * rows)
+        del x, o
+        torch.cuda.empty_cache()
     return 0
 
 

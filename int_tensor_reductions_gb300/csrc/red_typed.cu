@@ -319,8 +319,11 @@ int typed_rows_dt(const void *xv, int64_t rows, int64_t len, int accum, void *ou
         }
         return cuda_fail(e != cudaSuccess ? e : cudaGetLastError(), "red_rows_typed launch");
     }
+    // Lanes per row: the largest power of two (<= 32) that still leaves each
+    // lane TY_U whole 32-byte blocks of the row, so a lane keeps TY_U loads
+    // in flight (bf16 rows of 64 elements: 1 lane, not 4 lanes of one block).
     int g = 1;
-    while (g < 32 && (int64_t)g * 32 <= len)
+    while (g < 32 && (int64_t)(2 * g) * TY_U * epb<DT>() <= len)
         g *= 2;
     const int64_t rows_per_cta = (int64_t)(TY_NT / 32) * (32 / g);
     int64_t ctas = (rows + rows_per_cta - 1) / rows_per_cta;

@@ -17,7 +17,9 @@
 // idles).  Each lane owns V adjacent columns and keeps V running
 // accumulators (per-thread column accumulators); the lane groups of warp w
 // walk rows i0 + w*32/lpr, ... in steps of 16*32/lpr rows, each lane reading
-// 32 bytes of a row per load (coalesced, row-major order kept).  The row
+// 32 bytes of a row per load (16 bytes for 16-bit types, whose lanes then
+// keep 8 rows in flight instead of 4; coalesced, row-major order kept).  The
+// loaded words stay raw until they are folded.  The row
 // groups of a warp meet in a butterfly, the 16 warps in shared memory (fixed
 // order).  gridDim.y CTAs split the rows; with more than one, the CTA
 // partials go to the workspace and the CTA that arrives last for its column
@@ -34,40 +36,57 @@ namespace {
 constexpr int CP_WY = 16;                // warps per CTA (row interleave)
 constexpr int CP_NT = 32 * CP_WY;
 
-// V elements of a row starting at element p, widened to A.  V * sizeof(T)
-// is 32 (256-bit load), 16 (128-bit load) or sizeof(T) (one element).
+// Raw 32-bit words of a lane's V elements of one row: V * sizeof(T) is 32
+// (256-bit load, 8 words), 16 (128-bit load, 4 words) or sizeof(T) (one
+// element in the low bits of one word).  Rows are held raw while in flight
+// and widened only when folded, so 16-bit types keep as many bytes in flight
+// per register as 32-bit ones.
 template <int DT, int V>
-__device__ __forceinline__ void load_row(const typename Elem<DT>::T *p, typename Elem<DT>::A (&v)[V])
+struct RawRow {
+    static constexpr int BYTES = V * (int)sizeof(typename Elem<DT>::T);
+    static constexpr int W = BYTES >= 16 ? BYTES / 4 : 1;
+};
+
+// rows in flight per thread: 128 bytes for the vector paths, 8 elements for
+// the one-element path
+template <int DT, int V>
+__host__ __device__ constexpr int cols_u()
+{
+    return RawRow<DT, V>::BYTES >= 16 ? 128 / RawRow<DT, V>::BYTES : 8;
+}
+
+template <int DT, int V>
+__device__ __forceinline__ void load_raw(const typename Elem<DT>::T *p, uint32_t (&w)[RawRow<DT, V>::W])
+{
+    using T = typename Elem<DT>::T;
+    constexpr int W = RawRow<DT, V>::W;
+    if constexpr (W == 8) {
+        ld8u(reinterpret_cast<const uint32_t *>(p), w);
+    } else if constexpr (W == 4) {
+        ld4u(reinterpret_cast<const uint32_t *>(p), w);
+    } else if constexpr (sizeof(T) == 4) {
+        w[0] = __ldg(reinterpret_cast<const unsigned int *>(p));
+    } else {
+        w[0] = __ldg(reinterpret_cast<const unsigned short *>(p));
+    }
+}
+
+// acc[k] = op(acc[k], element k of the raw row), elements in column order.
+template <int OP, int DT, int V>
+__device__ __forceinline__ void fold_raw(typename Elem<DT>::A (&acc)[V], const uint32_t (&w)[RawRow<DT, V>::W])
 {
     using E = Elem<DT>;
-    using T = typename E::T;
-    constexpr int BYTES = V * (int)sizeof(T);
-    if constexpr (BYTES == 32 || BYTES == 16) {
-        constexpr int W = BYTES / 4;
-        uint32_t w[W];
-        if constexpr (W == 8) {
-            uint32_t (&w8)[8] = w;
-            ld8u(reinterpret_cast<const uint32_t *>(p), w8);
-        } else {
-            uint32_t (&w4)[4] = w;
-            ld4u(reinterpret_cast<const uint32_t *>(p), w4);
-        }
-        if constexpr (sizeof(T) == 4) {
+    using K = Comb<OP, typename E::A>;
+    if constexpr (sizeof(typename E::T) == 4 || V == 1) {
 #pragma unroll
-            for (int k = 0; k < V; ++k)
-                v[k] = E::widen(w[k]);
-        } else {
-#pragma unroll
-            for (int k = 0; k < W; ++k) {
-                v[2 * k] = E::widen(w[k] & 0xffffu);
-                v[2 * k + 1] = E::widen(w[k] >> 16);
-            }
-        }
+        for (int k = 0; k < V; ++k)
+            acc[k] = K::op(acc[k], E::widen(w[k]));
     } else {
-        if constexpr (sizeof(T) == 4)
-            v[0] = E::widen(__ldg(reinterpret_cast<const unsigned int *>(p)));
-        else
-            v[0] = E::widen(__ldg(reinterpret_cast<const unsigned short *>(p)));
+#pragma unroll
+        for (int k = 0; k < V / 2; ++k) {
+            acc[2 * k] = K::op(acc[2 * k], E::widen(w[k] & 0xffffu));
+            acc[2 * k + 1] = K::op(acc[2 * k + 1], E::widen(w[k] >> 16));
+        }
     }
 }
 
@@ -81,7 +100,8 @@ cols_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t R, int64_t C, in
     using E = Elem<DT>;
     using A = typename E::A;
     using K = Comb<OP, A>;
-    constexpr int U = sizeof(typename E::T) == 4 ? 4 : 2;  // rows in flight per thread (128 bytes)
+    constexpr int U = cols_u<DT, V>();
+    constexpr int W = RawRow<DT, V>::W;
     __shared__ A s_p[CP_WY][32 * V];
     __shared__ int s_last;
 
@@ -102,25 +122,39 @@ cols_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t R, int64_t C, in
     for (int k = 0; k < V; ++k)
         p[k] = K::identity();
     if (live) {
-        const typename E::T *q = x + col;
-        int64_t i = i0 + (int64_t)wy * rpw + sub;
-        for (; i + (U - 1) * step < i1; i += U * step) {
-            A v[U][V];
+        // rows i0 + wy*rpw + sub, then every step-th row, below i1: walked as
+        // a pointer to the lane's columns of the row, rs elements per step
+        const int64_t i = i0 + (int64_t)wy * rpw + sub;
+        const typename E::T *r = x + i * ld + col;
+        const typename E::T *const end = x + i1 * ld + col;
+        const int64_t rs = step * ld;
+        for (; r + (U - 1) * rs < end; r += U * rs) {
+            uint32_t w[U][W];
 #pragma unroll
             for (int u = 0; u < U; ++u)
-                load_row<DT, V>(q + (i + u * step) * ld, v[u]);
+                load_raw<DT, V>(r + u * rs, w[u]);
 #pragma unroll
             for (int u = 0; u < U; ++u)
-#pragma unroll
-                for (int k = 0; k < V; ++k)
-                    p[k] = K::op(p[k], v[u][k]);
+                fold_raw<OP, DT, V>(p, w[u]);
         }
-        for (; i < i1; i += step) {
-            A v[V];
-            load_row<DT, V>(q + i * ld, v);
+        // the last (fewer than U) rows: a batch of U / 2, then one at a time
+        if constexpr (U >= 4) {
+            constexpr int H = U / 2;
+            if (r + (H - 1) * rs < end) {
+                uint32_t w[H][W];
 #pragma unroll
-            for (int k = 0; k < V; ++k)
-                p[k] = K::op(p[k], v[k]);
+                for (int u = 0; u < H; ++u)
+                    load_raw<DT, V>(r + u * rs, w[u]);
+#pragma unroll
+                for (int u = 0; u < H; ++u)
+                    fold_raw<OP, DT, V>(p, w[u]);
+                r += H * rs;
+            }
+        }
+        for (; r < end; r += rs) {
+            uint32_t w[W];
+            load_raw<DT, V>(r, w);
+            fold_raw<OP, DT, V>(p, w);
         }
     }
     // the row groups of the warp meet (butterfly over the group bits)
@@ -208,7 +242,7 @@ int launch_cols(const void *xv, int64_t R, int64_t C, int64_t ld, void *outv, cu
     const int occ = cached_occupancy(occ_cache, (const void *)cols_kernel<OP, DT, V>, CP_NT);
     if (occ <= 0)
         return fail(RED_ECUDA, "red_cols: kernel cannot be resident on this device");
-    constexpr int U = sizeof(T) == 4 ? 4 : 2;
+    constexpr int U = cols_u<DT, V>();
     // lanes per row: enough V-wide chunks for C columns, a power of two <= 32
     const int64_t chunks = (C + V - 1) / V;
     int lpr = 1;
@@ -282,7 +316,10 @@ int launch_cols_dt(const void *x, int64_t R, int64_t C, int64_t ld, void *out, c
     // vectors, so a lane's V columns never pass column C (neither the reads
     // of a row nor the writes to out).
     const int64_t row_bytes = ld * SZ, valid_bytes = C * SZ;
-    if (row_bytes % 32 == 0 && valid_bytes % 32 == 0 && a % 32 == 0)
+    // 16-bit types take 128-bit loads (8 columns and 8 rows in flight per
+    // lane) unless the lanes see too few rows to fill 8 loads each
+    const bool wide = SZ == 4 || R < (int64_t)CP_WY * 8;
+    if (wide && row_bytes % 32 == 0 && valid_bytes % 32 == 0 && a % 32 == 0)
         return launch_cols<OP, DT, 32 / SZ>(x, R, C, ld, out, s, di);
     if (row_bytes % 16 == 0 && valid_bytes % 16 == 0 && a % 16 == 0)
         return launch_cols<OP, DT, 16 / SZ>(x, R, C, ld, out, s, di);

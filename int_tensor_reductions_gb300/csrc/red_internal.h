@@ -55,6 +55,9 @@ int launch_ragged(int op, const float *x, const int64_t *off, int64_t rows, int6
                   float *out, cudaStream_t s);
 int launch_typed(bool full, int op, int dtype, const void *x, int64_t rows, int64_t len, int accum, void *out,
                  cudaStream_t s);
+// Rows of 2..32 bytes (len * element size dividing 32) from a 32-byte aligned x.
+int launch_typed_tiny(int op, int dtype, const void *x, int64_t rows, int len, int accum, void *out, cudaStream_t s,
+                      int sms);
 // Column reductions of the R x C region of a row-major matrix with row stride ld >= C.
 int launch_cols(int op, int dtype, const void *x, int64_t R, int64_t C, int64_t ld, void *out, cudaStream_t s);
 

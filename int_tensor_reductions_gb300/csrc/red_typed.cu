@@ -13,7 +13,8 @@
 // combines through a butterfly.  Full vector: the grid splits the blocks, the
 // CTA combines through a warp butterfly and shared memory, and the last CTA
 // to finish folds the CTA partials (last-block grid stage, workspace
-// partials).
+// partials).  Rows of 2, 4, 8, 16 or 32 bytes from a 32-byte aligned base
+// go to red_typed_tiny.cu instead (several rows per block).
 #include "red_internal.h"
 #include "red_prims.cuh"
 #include "red_types.cuh"
@@ -319,6 +320,10 @@ int typed_rows_dt(const void *xv, int64_t rows, int64_t len, int accum, void *ou
         }
         return cuda_fail(e != cudaSuccess ? e : cudaGetLastError(), "red_rows_typed launch");
     }
+    // Rows of 2, 4, 8, 16 or 32 bytes from a 32-byte aligned base: whole
+    // blocks per thread, several rows each.
+    if ((((uintptr_t)x) & 31u) == 0 && len <= epb<DT>() && epb<DT>() % len == 0)
+        return launch_typed_tiny(OP, DT, x, rows, (int)len, accum, out, s, sms);
     // Lanes per row: the largest power of two (<= 32) that still leaves each
     // lane TY_U whole 32-byte blocks of the row, so a lane keeps TY_U loads
     // in flight (bf16 rows of 64 elements: 1 lane, not 4 lanes of one block).

@@ -106,3 +106,32 @@ def test_int32_sum_wraps():
     """2^31 - 1 + 1 wraps to -2^31 in int32 (bit for bit with the oracle)."""
     x = torch.tensor([2**31 - 1, 1], dtype=torch.int32, device="cuda")
     assert int(itr.red_full_typed("sum", x)[0]) == -2**31
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("op", OPS)
+def test_rows_of_a_block_or_less(op, dtype):
+    """Rows of 2 to 32 bytes (one 32-byte block holds 1 to 16 of them) from a
+    32-byte aligned base, row counts that leave a partial block, results
+    written as vectors (aligned out) and element by element (out one element
+    off its alignment), with and without accum; the element just outside out
+    keeps its value."""
+    size = 2 if dtype in ("f16", "bf16", "i16", "u16") else 4
+    for length in (1, 2, 4, 8, 16):
+        if length * size > 32:
+            continue
+        for rows in (1, 15, 17, 1000, 100_003):
+            x = synth.col_input(op, dtype, (rows, length), rows + length, device="cuda")
+            assert x.data_ptr() % 32 == 0
+            old_full = synth.col_input(op, dtype, (rows + 1,), length, device="cuda")
+            for shift in (0, 1):
+                old = old_full[shift:shift + rows]
+                for accum in (False, True):
+                    buf = old_full.clone()  # the element outside out must not change
+                    out = buf[shift:shift + rows]
+                    itr.red_rows_typed(op, x, accum=accum, out=out, dtype=dtype)
+                    ref = oracle.rows_typed(op, dtype, _raw(x), rows, length, accum, _raw(old))
+                    what = f"{op} {dtype} {rows}x{length} shift={shift} accum={accum}"
+                    _compare(_decode(out, dtype), op, dtype, ref, what, length + 1)
+                    edge = 0 if shift else rows
+                    assert _raw(buf[edge:edge + 1]).tolist() == _raw(old_full[edge:edge + 1]).tolist(), what

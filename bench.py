@@ -216,11 +216,20 @@ def _case_inputs(name, dev):
         x = synth.col_input("max", "bf16", (65536, 2048), 12, dev)
         o = torch.empty(65536, dtype=x.dtype, device=dev)
         return (lambda: itr.red_rows_typed("max", x, out=o)), 2 * x.numel() + 2 * 65536
+    if name == "typed_rows_u16_max_2p24x8":
+        x = synth.col_input("max", "u16", (1 << 24, 8), 13, dev)
+        o = torch.empty(1 << 24, dtype=x.dtype, device=dev)
+        return (lambda: itr.red_rows_typed("max", x, out=o, dtype="u16")), 2 * x.numel() + 2 * (1 << 24)
+    if name == "cols_bf16_sum_131072x1024":
+        x = synth.col_input("sum", "bf16", (131072, 1024), 14, dev)
+        o = torch.empty(1024, dtype=x.dtype, device=dev)
+        return (lambda: itr.red_cols("sum", x, o)), 2 * x.numel() + 2 * 1024
     raise KeyError(name)
 
 
 CASES = ("stats_full_2p28", "stats_rows_65536x1024", "thread_rows_2p22x32", "cols_f16_prod_4096x16384",
-         "typed_full_f16_max_2p29", "typed_rows_bf16_max_65536x2048")
+         "typed_full_f16_max_2p29", "typed_rows_bf16_max_65536x2048", "typed_rows_u16_max_2p24x8",
+         "cols_bf16_sum_131072x1024")
 
 
 def run_case(args):

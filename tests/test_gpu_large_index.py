@@ -107,3 +107,32 @@ def test_typed_half_max_beyond_2p31():
     x[(1 << 31) + 1] = -2.0
     assert float(itr.red_full_typed("max", x)[0]) == 3.5
     assert float(itr.red_full_typed("min", x)[0]) == -2.0
+
+
+def test_cols_16bit_beyond_2p31():
+    """A (2**16 + 3) x (2**15 + 16) bfloat16 column max (128-bit loads, 8 rows
+    in flight per lane): zeros with markers in rows whose elements lie past
+    2**31."""
+    R, C = (1 << 16) + 3, (1 << 15) + 16
+    x = torch.zeros((R, C), dtype=torch.bfloat16, device="cuda")
+    x[R - 1, C - 1] = 5.0
+    x[R - 2, 7] = 3.0
+    x[(1 << 31) // C + 1, 100] = 2.0
+    m = itr.red_cols("max", x).to(torch.float64).cpu().numpy()
+    want = np.zeros(C)
+    want[C - 1], want[7], want[100] = 5.0, 3.0, 2.0
+    assert np.array_equal(m, want)
+
+
+def test_typed_short_rows_beyond_2p31():
+    """2**28 + 3 uint16 rows of 8 (two rows per 32-byte block, the last row
+    after the last whole block): markers in rows past element 2**31."""
+    rows = (1 << 28) + 3
+    x = torch.zeros((rows, 8), dtype=torch.int16, device="cuda")
+    marks = {rows - 1: 7, rows - 2: 9, (1 << 28) + 0: 11, (1 << 28) - 1: 13}
+    for r, v in marks.items():
+        x[r, 5] = v
+    out = itr.red_rows_typed("max", x, dtype="u16")
+    assert int((out != 0).sum()) == len(marks)
+    for r, v in marks.items():
+        assert int(out[r]) == v, r

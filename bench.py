@@ -881,7 +881,7 @@ def run_sweep(args):
         emit("red_rows sum", [rows, length], lambda: itr.red_rows("sum", x, out=o), 4 * rows * length + 4 * rows)
         del x, o
         torch.cuda.empty_cache()
-    for mean in (4, 24, 100, 1000):
+    for mean in (4, 8, 24, 100, 1000):
         rows = (1 << 27) // mean
         off = synth.ragged_offsets(rows, max(1, mean // 2), mean + mean // 2, 3, dev)
         nnz = int(off[-1].item())

@@ -103,7 +103,8 @@ enum red_knob {
     RED_KNOB_ROWS_GROUP = 1,   /* lanes per dense row: 1, 2, 4, 8, 16 or 32 */
     RED_KNOB_RAGGED_GROUP = 2, /* lanes per ragged row: 1, 2, 4, 8, 16 or 32 */
     RED_KNOB_COLPROD_SPLITS = 3, /* CTAs along the row axis of red_cols / red_colprod (>= 1) */
-    RED_KNOB_FULL_CTAS_PER_SM = 4 /* resident CTAs per SM for red_full (>= 1) */
+    RED_KNOB_FULL_CTAS_PER_SM = 4, /* resident CTAs per SM for red_full (>= 1) */
+    RED_KNOB_RAGGED_STAGED = 5 /* red_rows_ragged mapping: 1 CTA-staged tiles, 2 direct (lanes per row) */
 };
 
 /*
@@ -194,6 +195,11 @@ int red_rows_thread(int op, const float *x, int64_t rows, int len, int accum, fl
  *   out      device pointer to rows floats (read first when accum != 0).
  * An empty row gives 0 for RED_SUM, -inf for RED_MAX and +inf for RED_MIN
  * (the identity of the fold); with accum the old out[r] is kept.
+ * Mapping ("Row mapping (ragged rows)": thread per row with direct loads, or
+ * a CTA-staged copy of a row range into shared memory, chosen by
+ * measurement): rows of fewer than 11 floats on average go through
+ * shared-memory tiles, longer ones to lanes per row with direct loads;
+ * RED_KNOB_RAGGED_STAGED forces either.
  */
 int red_rows_ragged(int op, const float *x, const int64_t *offsets, int64_t rows, int64_t nnz,
                     int accum, float *out, red_stream_t stream);

@@ -351,6 +351,10 @@ int red_set_knob(int k, int value)
         if (value < 0 || value > 32)
             return fail(RED_EINVAL, "red_set_knob: CTAs per SM must be in 0..32");
         break;
+    case RED_KNOB_RAGGED_STAGED:
+        if (value < 0 || value > 2)
+            return fail(RED_EINVAL, "red_set_knob: ragged mapping must be 0 (auto), 1 (staged) or 2 (direct)");
+        break;
     default:
         return fail(RED_EINVAL, "red_set_knob: unknown knob %d", k);
     }
@@ -360,7 +364,7 @@ int red_set_knob(int k, int value)
 
 int red_get_knob(int k)
 {
-    if (k < RED_KNOB_ROWS_GROUP || k > RED_KNOB_FULL_CTAS_PER_SM)
+    if (k < RED_KNOB_ROWS_GROUP || k > RED_KNOB_RAGGED_STAGED)
         return fail(RED_EINVAL, "red_get_knob: unknown knob %d", k);
     return knob(k);
 }

@@ -55,6 +55,9 @@ int launch_ragged(int op, const float *x, const int64_t *off, int64_t rows, int6
                   float *out, cudaStream_t s);
 int launch_typed(bool full, int op, int dtype, const void *x, int64_t rows, int64_t len, int accum, void *out,
                  cudaStream_t s);
+// Ragged rows through shared-memory tiles (short rows).
+int launch_ragged_staged(int op, const float *x, const int64_t *off, int64_t rows, int64_t nnz, int accum,
+                         float *out, cudaStream_t s, int sms);
 // Rows of 2..32 bytes (len * element size dividing 32) from a 32-byte aligned x.
 int launch_typed_tiny(int op, int dtype, const void *x, int64_t rows, int len, int accum, void *out, cudaStream_t s,
                       int sms);

@@ -106,6 +106,10 @@ def test_knobs_and_modes(lib):
     itr.red_set_knob(itr.RED_KNOB_ROWS_GROUP, 8)
     assert itr.red_get_knob(itr.RED_KNOB_ROWS_GROUP) == 8
     itr.red_set_knob(itr.RED_KNOB_ROWS_GROUP, 0)
+    assert lib.red_set_knob(itr.RED_KNOB_RAGGED_STAGED, 3) == itr.RED_EINVAL
+    for v in (1, 2, 0):
+        itr.red_set_knob(itr.RED_KNOB_RAGGED_STAGED, v)
+        assert itr.red_get_knob(itr.RED_KNOB_RAGGED_STAGED) == v
     assert lib.red_get_knob(99) == itr.RED_EINVAL
 
 

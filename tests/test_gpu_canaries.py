@@ -85,6 +85,36 @@ def test_rows_thread_stats(rows, length):
     _intact(buf, 4 * rows, 0, f"red_rows_stats {rows}x{length}")
 
 
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_ragged_invalid_offsets_stay_inside(mode):
+    """Offsets that decrease, go negative or pass nnz (results unspecified,
+    the call succeeds): x is a slice of a sentinel-padded buffer, and
+    neither the padding around out nor any value beyond x may show up; both
+    mappings (staged tiles, lanes per row) and the automatic choice."""
+    itr.red_set_knob(itr.RED_KNOB_RAGGED_STAGED, mode)
+    try:
+        nnz = 3000
+        xbuf = torch.full((nnz + 2 * PAD,), 1e30, device="cuda")
+        x = xbuf[PAD:PAD + nnz]
+        x.copy_(synth.uniform((nnz,), -1.0, 1.0, 5, device="cuda"))
+        gen = np.random.default_rng(7)
+        off = np.cumsum(gen.integers(0, 6, size=1201)).astype(np.int64)
+        off[100:110] = off[100:110][::-1].copy()  # decreasing pairs
+        off[300] = -50
+        off[500] = nnz + 1000
+        off[900:] += 2 * nnz  # past the end
+        offd = torch.from_numpy(off).cuda()
+        for op in ("sum", "max", "min"):
+            buf, out = _guarded(off.size - 1, torch.float32, shift=1)
+            itr.red_rows_ragged(op, x, offd, out=out)
+            _intact(buf, off.size - 1, 1, f"red_rows_ragged {op} mode={mode} invalid offsets")
+            got = out.cpu().numpy()
+            finite = got[np.isfinite(got)]
+            assert (np.abs(finite) < 1e29).all(), "a value from outside x was read"
+    finally:
+        itr.red_set_knob(itr.RED_KNOB_RAGGED_STAGED, 0)
+
+
 def test_ragged_with_empty_rows():
     lens = np.random.default_rng(3).integers(0, 41, size=2001)
     lens[::7] = 0

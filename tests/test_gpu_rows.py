@@ -151,6 +151,38 @@ def test_ragged_lengths_8_to_40_every_remainder():
     _ragged_case(x, torch.from_numpy(off).cuda(), dst, "lengths 8..40")
 
 
+@pytest.mark.parametrize("g", [0, 1, 2, 4, 8])
+def test_ragged_lengths_1_to_7_every_alignment(g):
+    """Rows of 1..7 values at every start alignment 0..7 (inside one 32-byte
+    block, or across one boundary), 9 rounds of them (several warps' worth)."""
+    itr.red_set_knob(itr.RED_KNOB_RAGGED_GROUP, g)
+    try:
+        lens = np.array([L for _ in range(9) for L in range(1, 8) for _ in range(8)], np.int64)
+        _ragged_case(*_ragged_from_lengths(lens, 0, 81 + g), f"G={g} lengths 1..7")
+    finally:
+        itr.red_set_knob(itr.RED_KNOB_RAGGED_GROUP, 0)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_ragged_staged_and_direct_mappings(mode):
+    """Both mappings of the ragged rows (1: CTA-staged tiles, 2: lanes per
+    row) on short and empty rows, short rows around rows longer than the
+    staged buffer (8192 floats), 8..40-value rows (a tile needs several
+    staged runs) and one huge row, at two base alignments."""
+    itr.red_set_knob(itr.RED_KNOB_RAGGED_STAGED, mode)
+    try:
+        gen = np.random.default_rng(90 + mode)
+        long_among_short = gen.integers(0, 8, size=4000)
+        long_among_short[[5, 1500, 1501, 3000]] = [20000, 9000, 8190, 600]
+        cases = {"0..7": gen.integers(0, 8, size=5000), "long among short": long_among_short,
+                 "8..40": gen.integers(8, 41, size=2100), "one huge row": np.array([200_000])}
+        for name, lens in cases.items():
+            for shift in (0, 3):
+                _ragged_case(*_ragged_from_lengths(lens, shift, 91), f"mode={mode} {name} shift={shift}")
+    finally:
+        itr.red_set_knob(itr.RED_KNOB_RAGGED_STAGED, 0)
+
+
 def _ragged_from_lengths(lens, shift, seed):
     off = np.zeros(len(lens) + 1, np.int64)
     off[1:] = np.cumsum(lens)

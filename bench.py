@@ -224,12 +224,18 @@ def _case_inputs(name, dev):
         x = synth.col_input("sum", "bf16", (131072, 1024), 14, dev)
         o = torch.empty(1024, dtype=x.dtype, device=dev)
         return (lambda: itr.red_cols("sum", x, o)), 2 * x.numel() + 2 * 1024
+    if name == "ragged_short_2p25":
+        off = synth.ragged_offsets(1 << 25, 2, 6, 15, dev)
+        nnz = int(off[-1].item())
+        x = synth.uniform((nnz,), -1.0, 1.0, 16, dev)
+        o = torch.empty(1 << 25, device=dev)
+        return (lambda: itr.red_rows_ragged("sum", x, off, out=o)), 4 * nnz + 8 * ((1 << 25) + 1) + 4 * (1 << 25)
     raise KeyError(name)
 
 
 CASES = ("stats_full_2p28", "stats_rows_65536x1024", "thread_rows_2p22x32", "cols_f16_prod_4096x16384",
          "typed_full_f16_max_2p29", "typed_rows_bf16_max_65536x2048", "typed_rows_u16_max_2p24x8",
-         "cols_bf16_sum_131072x1024")
+         "cols_bf16_sum_131072x1024", "ragged_short_2p25")
 
 
 def run_case(args):

@@ -199,7 +199,8 @@ int red_rows_thread(int op, const float *x, int64_t rows, int len, int accum, fl
  * a CTA-staged copy of a row range into shared memory, chosen by
  * measurement): rows of fewer than 11 floats on average go through
  * shared-memory tiles, longer ones to lanes per row with direct loads;
- * RED_KNOB_RAGGED_STAGED forces either.
+ * RED_KNOB_RAGGED_STAGED forces either, and a RED_KNOB_RAGGED_GROUP setting
+ * (lanes per row) implies the direct mapping unless staging is forced.
  */
 int red_rows_ragged(int op, const float *x, const int64_t *offsets, int64_t rows, int64_t nnz,
                     int accum, float *out, red_stream_t stream);

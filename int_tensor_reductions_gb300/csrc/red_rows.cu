@@ -311,9 +311,11 @@ int launch_ragged(int op, const float *x, const int64_t *off, int64_t rows, int6
     if (st != RED_OK)
         return st;
     // Short rows (mean below RAGGED_STAGED_MEAN floats) through shared-memory
-    // tiles, longer ones with lanes per row and direct loads.
+    // tiles, longer ones with lanes per row and direct loads; a lanes-per-row
+    // setting asks for the direct mapping.
     const int mode = knob(RED_KNOB_RAGGED_STAGED);
-    const bool staged = mode == 1 || (mode == 0 && rows > 0 && nnz < RAGGED_STAGED_MEAN * rows);
+    const bool staged = mode == 1 || (mode == 0 && knob(RED_KNOB_RAGGED_GROUP) == 0 && rows > 0 &&
+                                      nnz < RAGGED_STAGED_MEAN * rows);
     if (staged)
         return launch_ragged_staged(op, x, off, rows, nnz, accum, out, s, di.sms);
     const int g = knob(RED_KNOB_RAGGED_GROUP) ? knob(RED_KNOB_RAGGED_GROUP)

@@ -912,7 +912,8 @@ def run_sweep(args):
         torch.cuda.empty_cache()
     for dtype, shape in (("f16", (1 << 28,)), ("i32", (1 << 27,)), ("bf16", (1 << 22, 64)), ("i32", (1 << 23, 16)),
                          ("f16", (4096, 1 << 16)), ("u16", (1 << 24, 8)), ("i32", (1 << 26, 2)),
-                         ("u16", (1 << 27, 1)), ("bf16", (1 << 23, 16)), ("f32", (1 << 25, 4))):
+                         ("u16", (1 << 27, 1)), ("bf16", (1 << 23, 16)), ("f32", (1 << 25, 4)),
+                         ("bf16", (1 << 21, 128)), ("f32", (1 << 21, 64)), ("i32", (1 << 19, 256))):
         x = synth.col_input("max", dtype, shape, 7, dev)
         if len(shape) == 1:
             o = torch.empty(1, dtype=x.dtype, device=dev)

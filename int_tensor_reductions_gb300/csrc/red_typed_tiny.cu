@@ -1,8 +1,10 @@
 // red_typed_tiny.cu -- per-row sum / max / min / product (with accum) of
-// typed rows that are 2, 4, 8, 16 or 32 bytes long, from a 32-byte aligned
-// base: several whole rows per 256-bit block, so a thread keeps four
+// short typed rows from a 32-byte aligned base.  Rows of 2, 4, 8, 16 or 32
+// bytes: several whole rows per 256-bit block, so a thread keeps four
 // 32-byte loads in flight however short the rows are, and the results of a
-// block leave as one vector store.  Same operation and arithmetic as the row
+// block leave as one vector store.  Rows of 2, 4 or 8 whole blocks (64 to
+// 256 bytes): the blocks of the matrix read in order across the lanes, a
+// row's blocks meeting in a butterfly over the lanes that hold them.  Same operation and arithmetic as the row
 // kernel of red_typed.cu (Apache TVM docs, "reduction -> sm100_packed", "How
 // inputs change the algorithm": the old dst value is one more operand); a
 // 32-bit accumulator per element type, one narrowing at the end.
@@ -128,6 +130,75 @@ typed_tiny_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t rows, int 
     }
 }
 
+// Rows of RB whole 32-byte blocks (RB = 2, 4 or 8: 64 to 256 bytes) from a
+// 32-byte aligned base: the matrix is one run of rows * RB blocks
+// read grid-stride, TY_U blocks in flight per thread, so that consecutive
+// lanes read consecutive blocks (every warp load is 1 KB contiguous) and the
+// RB blocks of a row sit in RB consecutive lanes (the warp's first block
+// index is a multiple of 32, hence of RB).  Each lane folds its block, the RB
+// lanes of a row meet in a butterfly, and the row's first lane folds the
+// accum value in and writes the result.
+template <int OP, int DT, int RB>
+__global__ void __launch_bounds__(TY_NT)
+typed_blockrows_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t rows, int accum,
+                       typename Elem<DT>::T *__restrict__ out)
+{
+    pdl_enter();
+    using E = Elem<DT>;
+    using A = typename E::A;
+    using K = Comb<OP, A>;
+    static_assert(RB == 2 || RB == 4 || RB == 8, "blocks per row");
+    const int lane = threadIdx.x & 31;
+    const int64_t nblk = rows * RB;
+    const int64_t tid = (int64_t)blockIdx.x * TY_NT + threadIdx.x;
+    const int64_t nth = (int64_t)gridDim.x * TY_NT;
+    for (int64_t c0 = tid; c0 - lane < nblk; c0 += (int64_t)TY_U * nth) {  // warp-uniform
+        uint32_t w[TY_U][8];  // all loads out before any fold
+#pragma unroll
+        for (int u = 0; u < TY_U; ++u)
+            if (c0 + u * nth < nblk)
+                ld8u(reinterpret_cast<const uint32_t *>(x + (c0 + u * nth) * epb<DT>()), w[u]);
+#pragma unroll
+        for (int u = 0; u < TY_U; ++u) {
+            const int64_t b = c0 + u * nth;
+            A acc = K::identity();
+            if (b < nblk)
+#pragma unroll
+                for (int j = 0; j < epb<DT>(); ++j)
+                    acc = K::op(acc, block_elem<DT>(w[u], j));
+#pragma unroll
+            for (int o = 1; o < RB; o <<= 1)
+                acc = K::op(acc, __shfl_xor_sync(0xffffffffu, acc, o));
+            if (b < nblk && (lane & (RB - 1)) == 0) {
+                const int64_t r = b / RB;
+                if (accum)
+                    acc = K::op(E::widen(bits_of<DT>(out[r])), acc);
+                out[r] = E::narrow(acc);
+            }
+        }
+    }
+}
+
+template <int OP, int DT, int RB>
+int launch_blockrows(const typename Elem<DT>::T *x, int64_t rows, int accum, typename Elem<DT>::T *out, cudaStream_t s,
+                     int sms)
+{
+    static std::atomic<int> occ_cache{0};
+    const int occ = cached_occupancy(occ_cache, (const void *)typed_blockrows_kernel<OP, DT, RB>, TY_NT);
+    if (occ <= 0)
+        return fail(RED_ECUDA, "red_rows_typed: kernel cannot be resident on this device");
+    const int64_t need = (rows * RB + (int64_t)TY_NT * TY_U - 1) / ((int64_t)TY_NT * TY_U);
+    int64_t ctas = (int64_t)sms * occ;
+    if (need < ctas)
+        ctas = need;
+    if (ctas < 1)
+        ctas = 1;
+    const cudaError_t e =
+        launch_pdl(typed_blockrows_kernel<OP, DT, RB>, dim3((unsigned)ctas), dim3(TY_NT), s, x, rows, accum, out);
+    count_launches(1);
+    return cuda_fail(e != cudaSuccess ? e : cudaGetLastError(), "red_rows_typed launch");
+}
+
 template <int OP, int DT, int NE>
 int launch_tiny(const typename Elem<DT>::T *x, int64_t rows, int accum, typename Elem<DT>::T *out, cudaStream_t s,
                 int sms)
@@ -155,6 +226,13 @@ template <int OP, int DT>
 int typed_tiny_dt(const typename Elem<DT>::T *x, int64_t rows, int len, int accum, typename Elem<DT>::T *out,
                   cudaStream_t s, int sms)
 {
+    if (len > epb<DT>()) {  // whole blocks per row
+        switch (len / epb<DT>()) {
+        case 2: return launch_blockrows<OP, DT, 2>(x, rows, accum, out, s, sms);
+        case 4: return launch_blockrows<OP, DT, 4>(x, rows, accum, out, s, sms);
+        default: return launch_blockrows<OP, DT, 8>(x, rows, accum, out, s, sms);
+        }
+    }
     switch (len) {
     case 1: return launch_tiny<OP, DT, 1>(x, rows, accum, out, s, sms);
     case 2: return launch_tiny<OP, DT, 2>(x, rows, accum, out, s, sms);

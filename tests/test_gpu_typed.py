@@ -111,16 +111,17 @@ def test_int32_sum_wraps():
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("op", OPS)
 def test_rows_of_a_block_or_less(op, dtype):
-    """Rows of 2 to 32 bytes (one 32-byte block holds 1 to 16 of them) from a
-    32-byte aligned base, row counts that leave a partial block, results
+    """Rows of 2 to 32 bytes (one 32-byte block holds 1 to 16 of them) and of
+    2 to 32 whole blocks, from a 32-byte aligned base, row counts that leave
+    a partial block or a partial warp of blocks, results
     written as vectors (aligned out) and element by element (out one element
     off its alignment), with and without accum; the element just outside out
     keeps its value."""
     size = 2 if dtype in ("f16", "bf16", "i16", "u16") else 4
-    for length in (1, 2, 4, 8, 16):
-        if length * size > 32:
+    for length in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512):
+        if length * size > 1024:
             continue
-        for rows in (1, 15, 17, 1000, 100_003):
+        for rows in ((1, 15, 17, 1000, 100_003) if length * size <= 32 else (1, 3, 33, 1000, 20_003)):
             x = synth.col_input(op, dtype, (rows, length), rows + length, device="cuda")
             assert x.data_ptr() % 32 == 0
             old_full = synth.col_input(op, dtype, (rows + 1,), length, device="cuda")

@@ -929,7 +929,7 @@ def run_sweep(args):
     o = torch.empty(4, device=dev)
     emit("red_full_stats", [1 << 28], lambda: itr.red_full_stats(x, o), 4 * (1 << 28) + 16)
     del x, o
-    for rows, length in ((1 << 23, 16), (1 << 21, 64), (1 << 17, 1024)):
+    for rows, length in ((1 << 23, 16), (1 << 22, 32), (1 << 21, 64), (1 << 17, 1024)):
         x = synth.uniform((rows, length), -1.0, 1.0, 9, dev)
         o = torch.empty((rows, 4), device=dev)
         emit("red_rows_stats", [rows, length], lambda: itr.red_rows_stats(x, o), 4 * rows * length + 16 * rows)

@@ -232,8 +232,19 @@ rows_stats_kernel(const float *__restrict__ x, int64_t rows, int64_t len, float 
                             st.chunk(v[u]);
                 }
             } else {
-                for (int64_t k = b + gl; k < e; k += G)  // the row inside one 32-byte block
-                    st.scalar(ld1(x + k));
+                // the row inside one 32-byte block (fewer than 8 floats):
+                // every load of the lane out before any fold
+                constexpr int KMAX = (7 + G - 1) / G;
+                float t[KMAX];
+#pragma unroll
+                for (int k = 0; k < KMAX; ++k) {
+                    const int64_t i = b + gl + (int64_t)k * G;
+                    t[k] = i < e ? ld1(x + i) : 0.0f;
+                }
+#pragma unroll
+                for (int k = 0; k < KMAX; ++k)
+                    if (b + gl + (int64_t)k * G < e)
+                        st.scalar(t[k]);
             }
         }
         const float s = group_tree<OP_SUM, G>(st.sum.finish());
@@ -243,6 +254,63 @@ rows_stats_kernel(const float *__restrict__ x, int64_t rows, int64_t len, float 
         if (live && gl == 0)
             *reinterpret_cast<float4 *>(out + 4 * r) = make_float4(s, m, n, a);
     }
+}
+
+// Rows of RB whole 32-byte blocks (RB = 2, 4 or 8: 16, 32 or 64 floats)
+// from a 32-byte aligned base: the matrix read as one run of rows * RB
+// blocks, grid-stride, SR_U blocks in flight per thread, consecutive lanes
+// on consecutive blocks (every warp load 1 KB contiguous); a row's blocks
+// sit in RB consecutive lanes (the warp's first block index is a multiple
+// of 32), which meet in four butterflies; the row's first lane writes.
+template <int RB>
+__global__ void __launch_bounds__(SR_NT)
+rows_stats_blocks_kernel(const float *__restrict__ x, int64_t rows, float *__restrict__ out)
+{
+    pdl_enter();
+    static_assert(RB == 2 || RB == 4 || RB == 8, "blocks per row");
+    const int lane = threadIdx.x & 31;
+    const int64_t nblk = rows * RB;
+    const int64_t tid = (int64_t)blockIdx.x * SR_NT + threadIdx.x;
+    const int64_t nth = (int64_t)gridDim.x * SR_NT;
+    for (int64_t c0 = tid; c0 - lane < nblk; c0 += (int64_t)SR_U * nth) {  // warp-uniform
+        float v[SR_U][8];
+#pragma unroll
+        for (int u = 0; u < SR_U; ++u)
+            if (c0 + u * nth < nblk)
+                ld8(x + 8 * (c0 + u * nth), v[u]);
+#pragma unroll
+        for (int u = 0; u < SR_U; ++u) {
+            const int64_t b = c0 + u * nth;
+            Stats4 st;
+            st.init();
+            if (b < nblk)
+                st.chunk(v[u]);
+            const float s = group_tree<OP_SUM, RB>(st.sum.finish());
+            const float m = group_tree<OP_MAX, RB>(st.mx.finish());
+            const float n = group_tree<OP_MIN, RB>(st.mn.finish());
+            const float a = group_tree<OP_SUM, RB>(st.asum.finish());
+            if (b < nblk && (lane & (RB - 1)) == 0)
+                *reinterpret_cast<float4 *>(out + 4 * (b / RB)) = make_float4(s, m, n, a);
+        }
+    }
+}
+
+template <int RB>
+int launch_rows_stats_blocks(const float *x, int64_t rows, float *out, cudaStream_t s, int sms)
+{
+    static std::atomic<int> occ_cache{0};
+    const int occ = cached_occupancy(occ_cache, (const void *)rows_stats_blocks_kernel<RB>, SR_NT);
+    if (occ <= 0)
+        return fail(RED_ECUDA, "red_rows_stats: kernel cannot be resident on this device");
+    const int64_t need = (rows * RB + (int64_t)SR_NT * SR_U - 1) / ((int64_t)SR_NT * SR_U);
+    int64_t ctas = (int64_t)sms * occ;
+    if (need < ctas)
+        ctas = need;
+    if (ctas < 1)
+        ctas = 1;
+    const cudaError_t e = launch_pdl(rows_stats_blocks_kernel<RB>, dim3((unsigned)ctas), dim3(SR_NT), s, x, rows, out);
+    count_launches(1);
+    return cuda_fail(e != cudaSuccess ? e : cudaGetLastError(), "red_rows_stats launch");
 }
 
 template <int G>
@@ -269,6 +337,15 @@ int launch_rows_stats(const float *x, int64_t rows, int64_t len, float *out, cud
     const int st = device_info(&di);
     if (st != RED_OK)
         return st;
+    // rows of 16, 32 or 64 floats from a 32-byte aligned base: consecutive
+    // lanes on consecutive blocks of the matrix
+    if ((((uintptr_t)x) & 31u) == 0 && (len == 16 || len == 32 || len == 64)) {
+        switch (len) {
+        case 16: return launch_rows_stats_blocks<2>(x, rows, out, s, di.sms);
+        case 32: return launch_rows_stats_blocks<4>(x, rows, out, s, di.sms);
+        default: return launch_rows_stats_blocks<8>(x, rows, out, s, di.sms);
+        }
+    }
     int g = 1;  // about 32 floats per lane
     while (g < 32 && (int64_t)g * 64 <= len)
         g *= 2;

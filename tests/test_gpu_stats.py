@@ -75,7 +75,9 @@ def _check_rows(x2d: torch.Tensor, what: str):
     check_sum(got[:, 3], a, a, what + " sum|x|")
 
 
-@pytest.mark.parametrize("rows,length", [(1, 1), (5, 7), (33, 8), (100, 24), (257, 41), (64, 1024), (9, 5000)])
+@pytest.mark.parametrize("rows,length", [(1, 1), (5, 7), (33, 8), (100, 24), (257, 41), (64, 1024), (9, 5000),
+                                         (300, 3), (1000, 5), (1, 16), (3, 16), (4099, 16), (17, 32),
+                                         (2049, 32), (1000, 64), (33, 64)])
 def test_rows_stats_shapes(rows, length):
     x = synth.uniform((rows * length + 3,), -4.0, 4.0, rows + length, device="cuda")
     _check_rows(x[:rows * length].view(rows, length), f"{rows}x{length}")

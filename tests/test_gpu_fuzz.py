@@ -1,4 +1,4 @@
-"""Seeded random cases of every entry point against the oracle: sizes,
+"""Seeded random cases of the entry points against the oracle: sizes,
 base alignments, operators, element types, accum, row strides and every
 mapping choice (grid stage, lanes per row, ragged mapping, column row
 splits) drawn at random, so that combinations the hand-picked shapes of the
@@ -153,7 +153,7 @@ def test_typed_rows(case):
     gen = np.random.default_rng(5000 + case)
     dtype = DTYPES[int(gen.integers(0, len(DTYPES)))]
     op = ("sum", "max", "min", "prod")[int(gen.integers(0, 4))]
-    length = int(gen.choice([1, 2, 3, 4, 8, 16, 17, 64, 100, 1000, 5000]))
+    length = int(gen.choice([1, 2, 3, 4, 8, 16, 17, 32, 64, 128, 100, 1000, 5000]))
     rows = int(gen.integers(1, max(2, min(4000, 1_000_000 // length))))
     shift = int(gen.integers(0, 2))
     accum = bool(gen.integers(0, 2))
@@ -187,3 +187,22 @@ def test_thread_rows(case):
             check_exact(to_host(out), oracle.thread_rows_sum(xh, rows, length, accum, dh), what)
         else:
             check_exact(to_host(out), oracle.rows(op, xh, rows, length, accum, dh), what)
+
+
+@pytest.mark.parametrize("case", range(N_CASES))
+def test_rows_stats(case):
+    gen = np.random.default_rng(7000 + case)
+    length = int(gen.choice([1, 3, 7, 8, 16, 24, 32, 64, 65, 1024, 5000]))
+    rows = int(gen.integers(1, max(2, min(5000, 2_000_000 // length))))
+    shift = int(gen.choice([0, 0, 1, 3, 8]))
+    x = _shifted(synth.uniform((rows * length + 8,), -4.0, 4.0, case, device="cuda"), rows * length,
+                 shift).view(rows, length)
+    xh = to_host(x)
+    got = to_host(itr.red_rows_stats(x))
+    what = f"case {case}: {rows}x{length} shift={shift}"
+    s, a = oracle.rows("sum", xh, rows, length)
+    check_sum(got[:, 0], s, a, what + " sum")
+    check_exact(got[:, 1].copy(), oracle.rows("max", xh, rows, length), what + " max")
+    check_exact(got[:, 2].copy(), oracle.rows("min", xh, rows, length), what + " min")
+    check_sum(got[:, 3], a, a, what + " sum|x|")
+

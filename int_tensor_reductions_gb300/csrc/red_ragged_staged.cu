@@ -16,9 +16,10 @@
 // it copies the run's values with 128-bit loads of their 16-byte aligned
 // interior (at most three single floats at each end: every load inside the
 // span) and each thread folds its rows of the run from shared memory, the
-// old value first (accum), then the row's values in order.  A row that alone exceeds the buffer is folded by
-// the whole CTA (128-bit loads, a CTA reduction); a row whose offsets leave
-// the run's span (offsets that decrease) is folded from global memory.
+// old value first (accum), then the row's values in order.  A row that
+// alone exceeds the buffer is folded by the whole CTA (128-bit loads, a CTA
+// reduction, the old value combined with the result); a row whose offsets
+// leave the run's span (offsets that decrease) is folded from global memory.
 // With rows of a few floats, one lane per row spends ~10 L1 wavefronts per
 // 128 coalesced bytes on scattered 4-byte loads; the staged copy needs one.
 #include "red_internal.h"

@@ -448,28 +448,18 @@ def run_ours(args):
         step()
     torch.cuda.synchronize()
 
-    # (1) eager pass: per-op events around every call (the breakdown and the
-    # dominant kernel's launch durations)
+    # (1) eager pass (host-launched calls, no graph): its step time is
+    # reported beside the graph's
     K = args.steps
-    KE = min(K, 50)
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
-          for _ in range(KE)]
+    KE = min(K, 20)
     torch.cuda.synchronize()
     e_begin, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_begin.record(stream)
     for k in range(KE):
-        for i, (_, _, fn) in enumerate(calls):
-            ev[k][i][0].record(stream)
-            fn()
-            ev[k][i][1].record(stream)
+        step()
     e_end.record(stream)
     torch.cuda.synchronize()
     eager_ms = e_begin.elapsed_time(e_end) / KE
-    per_op = {}
-    for i, (name, key, _) in enumerate(calls):
-        ms = [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(KE)]
-        mean = sum(ms) / KE
-        per_op[name] = {"ms": round(mean, 5), "gbs": round(w.bytes_of[key] / (mean * 1e-3) / 1e9, 1)}
 
     # (2) the timed region: the step captured once as a CUDA graph (the same
     # library calls, no host launch gaps between them) and replayed K times
@@ -508,9 +498,12 @@ def run_ours(args):
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"] if peaks and "hbm_gbs" in peaks else FALLBACK_HBM_GBS
     peak_src = "measured" if peaks and "hbm_gbs" in peaks else "fallback"
+    # (3) per-op device time from CUDA graphs (each op's calls back to back)
+    per_op, ops_note = per_op_graphs(w, stream)
     dom = [per_op[n]["ms"] for n in ("full3 sum", "full3 max", "full3 min") if n in per_op]
     dom_ms = sum(dom) / len(dom) if dom else float("nan")
     achieved = w.bytes_of["full3"] / (dom_ms * 1e-3) / 1e9 if dom else None
+    ops_sum = sum(v["ms"] for v in per_op.values())
 
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
@@ -535,7 +528,8 @@ def run_ours(args):
         "ops": per_op,
         "timing": {"timed_region": f"CUDA graph of one step ({kernels_per_step} library kernels) replayed "
                                    f"{K} times", "eager_ms_per_step": round(eager_ms, 5),
-                   "ops_from": f"eager pass of {KE} steps with events around every call"},
+                   "ops_from": ops_note, "ops_sum_ms": round(ops_sum, 5),
+                   "ops_sum_over_ms_per_step": round(ops_sum / (total_ms / K), 4)},
         "gpu_launches": int(launches),
         "partial": {"only": only, "scale": args.scale} if partial else None,
         "clocks": clocks,
@@ -563,6 +557,70 @@ def run_ours(args):
         dist.barrier()
         dist.destroy_process_group()
     return 0
+
+
+def per_op_graphs(w, stream, calls_per_replay=16, replays=6):
+    """Device time per call of every op of the step, each timed alone: one
+    CUDA graph per op holding ``calls_per_replay`` back-to-back calls, over
+    copies of that op's inputs (so that every call reads its input cold: the
+    copies together exceed three times the L2; a replay calls every copy once), replayed ``replays`` times between
+    two events on the launching stream.  Graph replay leaves no host launch
+    gap, and programmatic dependent launch overlaps each call's launch with
+    its predecessor's drain, as in the timed region."""
+    import torch
+    import int_tensor_reductions_gb300 as itr
+    l2 = torch.cuda.get_device_properties(stream.device).L2_cache_size
+
+    def copies(t):
+        n = max(1, -(-3 * l2 // max(1, t.numel() * t.element_size())))
+        return [t] + [t.clone() for _ in range(n - 1)]
+
+    x1s, x2s, x4as, x4bs = copies(w.x1), copies(w.x2), copies(w.x4a), copies(w.x4b)
+    x3s, x5s = copies(w.x3), copies(w.x5)
+
+    def fns(name):
+        kind, op = name.split(" ")[0], name.split(" ")[1]
+        if kind == "full1":
+            return [lambda x=x: itr.red_full(op, x, w.o1[op]) for x in x1s]
+        if kind == "full3":
+            return [lambda x=x: itr.red_full(op, x, w.o3[op]) for x in x3s]
+        if kind == "rows2" and name.endswith("accum"):
+            return [lambda x=x: itr.red_rows("sum", x, accum=True, out=w.o2acc) for x in x2s]
+        if kind == "rows2":
+            return [lambda x=x: itr.red_rows(op, x, out=w.o2[op]) for x in x2s]
+        if kind == "ragged5":
+            return [lambda x=x: itr.red_rows_ragged(op, x, w.off5, out=w.o5[op]) for x in x5s]
+        if kind == "colprod4a":
+            return [lambda x=x: itr.red_colprod(x, w.o4a) for x in x4as]
+        return [lambda x=x: itr.red_colprod(x, w.o4b) for x in x4bs]
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    per_op = {}
+    for name, key in w.plan:
+        f = fns(name)
+        for fn in f:
+            fn()
+        torch.cuda.synchronize()
+        ncalls = max(calls_per_replay, len(f))
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for k in range(ncalls):
+                f[k % len(f)]()
+        g.replay()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(replays):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / (replays * ncalls)
+        per_op[name] = {"ms": round(ms, 5), "gbs": round(w.bytes_of[key] / (ms * 1e-3) / 1e9, 1)}
+        del g
+    del x1s, x2s, x4as, x4bs, x3s, x5s
+    torch.cuda.empty_cache()
+    note = (f"graph-timed per op: at least {calls_per_replay} back-to-back calls per CUDA graph over copies of the "
+            f"op's inputs (each call reads cold), {replays} replays between two events")
+    return per_op, note
 
 
 def compare_stages(w, stream, reps=10):
@@ -761,16 +819,21 @@ def column_ops(stream, dev, peak, reps=10):
 
 def typed_ops(stream, dev, peak, reps=10):
     """Full and row reductions of other element types (red_full_typed,
-    red_rows_typed) on inputs larger than L2: GB/s of algorithmic bytes."""
+    red_rows_typed) on inputs larger than L2: GB/s of algorithmic bytes; the
+    fp32 rows of the same shape through red_rows, timed the same way."""
     import torch
     import int_tensor_reductions_gb300 as itr
     from int_tensor_reductions_gb300 import synth
     res = {"unit": "GB/s", "note": "back-to-back calls replayed from a CUDA graph, inputs > L2"}
     cases = (("full", "sum", "i32", (1 << 28,)), ("full", "max", "f16", (1 << 29,)),
-             ("rows", "sum", "i32", (65536, 1024)), ("rows", "max", "bf16", (65536, 2048)))
+             ("rows", "sum", "i32", (65536, 1024)), ("rows", "sum", "f32", (65536, 1024)),
+             ("rows", "max", "bf16", (65536, 2048)))
     for kind, op, dtype, shape in cases:
         x = synth.col_input(op, dtype, shape, 12, dev)
-        if kind == "full":
+        if kind == "rows" and dtype == "f32":
+            o = torch.empty(shape[0], dtype=x.dtype, device=dev)
+            fn = lambda: itr.red_rows(op, x, out=o)  # noqa: E731
+        elif kind == "full":
             o = torch.empty(1, dtype=x.dtype, device=dev)
             fn = lambda: itr.red_full_typed(op, x, o, dtype=dtype)  # noqa: E731
         else:

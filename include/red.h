@@ -25,6 +25,8 @@
  *         implementation checks" (float and int32 among the element types).
  *
  * Conventions shared by every entry point
+ *   - Sizes are int64_t.  Every element count (n, rows * len, nnz, R * ld) is
+ *     at most 2^44; a larger one returns RED_EINVAL.
  *   - Pointers to data (x, offsets, out) are DEVICE pointers on the current
  *     CUDA device, owned by the caller, which keeps them alive until the work
  *     queued on `stream` has finished.  fp32 / int32 pointers must be 4-byte
@@ -50,7 +52,10 @@
  *     synchronise nothing).
  *     The counters reset themselves at the end of every call, so calls on one
  *     device must be ordered (one stream, or streams ordered by events):
- *     two such calls running at the same time on one device race.
+ *     two such calls running at the same time on one device race.  The
+ *     workspace lives in the device's primary context: after a
+ *     cudaDeviceReset the library must not be called on that device again in
+ *     the same process (its workspace pointers are stale).
  *   - fp32 sums use round-to-nearest with flush-to-zero packed adds and a
  *     library-chosen summation order: the result equals the exact sum up to
  *     rounding (tests bound it by 1e-5 * sum|x|).  Max / min are exact.
@@ -86,7 +91,9 @@ enum red_dtype {
     RED_U32 = 6
 };
 
-/* Status codes. */
+/* Status codes.  There is no timeout status: no kernel of this library
+ * waits on another CTA, stream or device (the last-block stages count
+ * arrivals and the last arrival does the fold), so no wait can run out. */
 enum red_status { RED_OK = 0, RED_EINVAL = -1, RED_ECUDA = -2, RED_ENOMEM = -3 };
 
 /* Grid stage of red_full (how the per-CTA partials become one scalar). */
@@ -104,7 +111,11 @@ enum red_knob {
     RED_KNOB_RAGGED_GROUP = 2, /* lanes per ragged row: 1, 2, 4, 8, 16 or 32 */
     RED_KNOB_COLPROD_SPLITS = 3, /* CTAs along the row axis of red_cols / red_colprod (>= 1) */
     RED_KNOB_FULL_CTAS_PER_SM = 4, /* resident CTAs per SM for red_full (>= 1) */
-    RED_KNOB_RAGGED_STAGED = 5 /* red_rows_ragged mapping: 1 CTA-staged tiles, 2 direct (lanes per row) */
+    RED_KNOB_RAGGED_STAGED = 5, /* red_rows_ragged mapping: 1 CTA-staged tiles, 2 direct (lanes per row) */
+    RED_KNOB_ROWS_ALIGNED = 6, /* red_rows on rows of whole 32-byte blocks: 2 = the general row kernel
+                                  instead of the aligned one (1 and 0: automatic) */
+    RED_KNOB_COLS_LANES = 7    /* red_cols / red_colprod: at most this many lanes per row of a column tile
+                                  (1, 2, 4, 8, 16 or 32) */
 };
 
 /*
@@ -113,7 +124,7 @@ enum red_knob {
  * shared-memory stage per CTA, then the grid stage set by red_set_full_mode.
  *   op     RED_SUM, RED_MAX or RED_MIN.
  *   x      device pointer to n contiguous floats (may be NULL when n == 0).
- *   n      number of elements, 0 <= n (n up to 2^40 is accepted).
+ *   n      number of elements, 0 <= n <= 2^44 (a larger n returns RED_EINVAL).
  *   out    device pointer to one float, written with the result.
  *   stream CUDA stream the work is queued on.
  * n == 0: RED_SUM writes 0; RED_MAX / RED_MIN return RED_EINVAL (an empty
@@ -289,7 +300,17 @@ int red_colprod(int dtype, const void *x, int64_t R, int64_t C, void *out, red_s
  * in all; the message says so.  n itself has no limit beyond red_full's.
  * Set-up: the first call on a device looks up the scratch array's device
  * address (cudaGetSymbolAddress, with that device current) and caches it, so
- * that first call should come before any CUDA stream capture.
+ * that first call should come before any CUDA stream capture.  The scratch
+ * array belongs to the library's device code, which the CUDA driver may load
+ * onto a device only when the library first uses that device (lazy module
+ * loading); the driver then places the module's code and static data, this
+ * array included, in device memory.  So "allocates nothing" holds from the
+ * moment the module is resident on the device: a caller that must not see
+ * even that load makes one call (or any other call of this library) on the
+ * device during its set-up.  A cudaDeviceReset, or any other teardown of the
+ * device's primary context, unloads the module and makes the cached address
+ * stale: this call must not be used on that device afterwards in the same
+ * process (red_full's workspace pointers are invalidated the same way).
  * Sharing: every call on a device uses the same scratch.  Each call first
  * clears the counter on its stream (cudaMemsetAsync, which allocates
  * nothing), and the partials are rewritten before they are read; calls that

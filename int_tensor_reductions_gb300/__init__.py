@@ -24,7 +24,8 @@ stream, or streams ordered by events): they share the library's workspace.
 """
 from ._binding import (  # noqa: F401
     RED_BF16, RED_EINVAL, RED_ECUDA, RED_ENOMEM, RED_F16, RED_F32, RED_I16, RED_I32, RED_KNOB_COLPROD_SPLITS,
-    RED_KNOB_FULL_CTAS_PER_SM, RED_KNOB_RAGGED_GROUP, RED_KNOB_RAGGED_STAGED, RED_KNOB_ROWS_GROUP, RED_MAX, RED_MIN,
+    RED_KNOB_FULL_CTAS_PER_SM, RED_KNOB_RAGGED_GROUP, RED_KNOB_RAGGED_STAGED, RED_KNOB_ROWS_ALIGNED, RED_KNOB_ROWS_GROUP,
+    RED_KNOB_COLS_LANES, RED_MAX, RED_MIN,
     RED_MODE_ATOMIC, RED_MODE_AUTO, RED_MODE_LAST_BLOCK, RED_MODE_TWO_PASS, RED_OK, RED_PROD, RED_SUM, RED_U16, RED_U32,
     RedError, lib, lib_path, red_colprod, red_cols, red_full, red_full_noalloc, red_full_stats, red_full_typed, red_get_full_mode, red_get_knob, red_last_error, red_launch_count,
     red_release_workspace, red_rows, red_rows_ragged, red_rows_stats, red_rows_thread, red_rows_typed, red_set_full_mode, red_set_knob, red_version,

@@ -12,6 +12,8 @@ RED_OK, RED_EINVAL, RED_ECUDA, RED_ENOMEM = 0, -1, -2, -3
 RED_MODE_AUTO, RED_MODE_TWO_PASS, RED_MODE_LAST_BLOCK, RED_MODE_ATOMIC = 0, 1, 2, 3
 RED_KNOB_ROWS_GROUP, RED_KNOB_RAGGED_GROUP, RED_KNOB_COLPROD_SPLITS, RED_KNOB_FULL_CTAS_PER_SM = 1, 2, 3, 4
 RED_KNOB_RAGGED_STAGED = 5
+RED_KNOB_ROWS_ALIGNED = 6
+RED_KNOB_COLS_LANES = 7
 
 _OPS = {"sum": RED_SUM, "max": RED_MAX, "min": RED_MIN, "prod": RED_PROD}
 # element type names of the column reductions and their sizes in bytes

@@ -22,7 +22,7 @@ std::atomic<int> g_sms[MAX_DEVICES];
 
 std::atomic<int> g_full_mode{RED_MODE_AUTO};
 std::atomic<uint64_t> g_launches{0};
-std::atomic<int> g_knobs[8];
+std::atomic<int> g_knobs[16];
 
 
 bool misaligned(const void *p, uintptr_t a) { return ((uintptr_t)p) % a != 0; }
@@ -103,7 +103,7 @@ int get_workspace(Workspace *ws)
 
 int knob(int which)
 {
-    if (which <= 0 || which >= 8)
+    if (which <= 0 || which >= 16)
         return 0;
     return g_knobs[which].load(std::memory_order_relaxed);
 }
@@ -355,6 +355,14 @@ int red_set_knob(int k, int value)
         if (value < 0 || value > 2)
             return fail(RED_EINVAL, "red_set_knob: ragged mapping must be 0 (auto), 1 (staged) or 2 (direct)");
         break;
+    case RED_KNOB_ROWS_ALIGNED:
+        if (value < 0 || value > 2)
+            return fail(RED_EINVAL, "red_set_knob: aligned-rows setting must be 0, 1 or 2");
+        break;
+    case RED_KNOB_COLS_LANES:
+        if (!(value == 0 || value == 1 || value == 2 || value == 4 || value == 8 || value == 16 || value == 32))
+            return fail(RED_EINVAL, "red_set_knob: lanes per row must be 0 or a power of two <= 32");
+        break;
     default:
         return fail(RED_EINVAL, "red_set_knob: unknown knob %d", k);
     }
@@ -364,7 +372,7 @@ int red_set_knob(int k, int value)
 
 int red_get_knob(int k)
 {
-    if (k < RED_KNOB_ROWS_GROUP || k > RED_KNOB_RAGGED_STAGED)
+    if (k < RED_KNOB_ROWS_GROUP || k > RED_KNOB_COLS_LANES)
         return fail(RED_EINVAL, "red_get_knob: unknown knob %d", k);
     return knob(k);
 }

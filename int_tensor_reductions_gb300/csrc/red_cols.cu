@@ -12,9 +12,9 @@
 // max / min compare values (signed or unsigned as the type is).
 //
 // Layout of the work: a CTA of 16 warps owns a tile of lpr*V adjacent
-// columns, lpr lanes per row (32, or the power of two that covers a narrower
-// matrix, whose warps then take 32/lpr consecutive rows per step, so no lane
-// idles).  Each lane owns V adjacent columns and keeps V running
+// columns, lpr lanes per row (8 for matrices of many rows, 32 for short ones,
+// or the power of two that covers a narrower matrix; the warps take 32/lpr
+// consecutive rows per step, so no lane idles).  Each lane owns V adjacent columns and keeps V running
 // accumulators (per-thread column accumulators); the lane groups of warp w
 // walk rows i0 + w*32/lpr, ... in steps of 16*32/lpr rows, each lane reading
 // 32 bytes of a row per load (16 bytes for 16-bit types, whose lanes then
@@ -23,8 +23,8 @@
 // groups of a warp meet in a butterfly, the 16 warps in shared memory (fixed
 // order).  gridDim.y CTAs split the rows; with more than one, the CTA
 // partials go to the workspace and the CTA that arrives last for its column
-// tile folds them, with all its lanes in a fixed order, into dst.  No CTA
-// ever waits for another.
+// tile folds them, with all its lanes in a fixed order, into dst (the
+// arrival is an acquire-release atomic, so no CTA fences or waits).
 #include "red_internal.h"
 #include "red_prims.cuh"
 #include "red_types.cuh"
@@ -187,14 +187,17 @@ cols_kernel(const typename Elem<DT>::T *__restrict__ x, int64_t R, int64_t C, in
 #pragma unroll
         for (int k = 0; k < V; ++k)
             part[(int64_t)blockIdx.y * C + col + k] = p[k];
-    __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0)
-        s_last = (atomicAdd(tick + blockIdx.x, 1u) == gridDim.y - 1);
+    if (threadIdx.x == 0) {
+        // release this CTA's partials (ordered before by the barrier) with the
+        // arrival; the last arrival acquires every other CTA's partials
+        unsigned prev;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(tick + blockIdx.x) : "memory");
+        s_last = prev == gridDim.y - 1;
+    }
     __syncthreads();
     if (!s_last)
         return;
-    __threadfence();
     // The last CTA folds the gridDim.y partials of its tile with all of its
     // lanes: row group g of warp w takes splits w*rpw+g, w*rpw+g + 16*rpw, ...
     // (a fixed assignment), then the groups meet in a butterfly and the warps
@@ -248,21 +251,35 @@ int launch_cols(const void *xv, int64_t R, int64_t C, int64_t ld, void *outv, cu
     int lpr = 1;
     while (lpr < 32 && lpr < chunks)
         lpr *= 2;
+    // At most 8 lanes per row (tiles of 8 * V columns, 128-256 bytes of a row
+    // per lane group) when every lane of an unsplit tile still keeps U rows in
+    // flight: narrow tiles are many enough to fill the GPU without splitting
+    // the rows, and a split costs a combine at the end of the launch (4096 x
+    // 16384: fp32 product 42.2 -> 40.0 us, f16 23.2 -> 21.1 us; 65536 x 1024
+    // fp32 sum 43.6 -> 41.2 us).  Short matrices keep wide tiles: a lane then
+    // still sees several rows (64 x 65536 int32: 3.9 us, 7.3 with 8 lanes).
+    if (lpr > 8 && RawRow<DT, V>::BYTES >= 16 && R >= (int64_t)CP_WY * 4 * U)
+        lpr = 8;
+    if (knob(RED_KNOB_COLS_LANES) > 0 && lpr > knob(RED_KNOB_COLS_LANES))
+        lpr = knob(RED_KNOB_COLS_LANES);
     const int rpw = 32 / lpr;
     const int64_t tile_cols = (int64_t)lpr * V;
     const int64_t tiles = (C + tile_cols - 1) / tile_cols;
     if (tiles > 0x7fffffffLL)
         return fail(RED_EINVAL, "red_cols: C too large");
-    // Row splits (each warp keeps at least U rows).  A wave of CTAs carries
-    // a fixed cost of a few microseconds (the CTAs' ramp, the split
-    // combine), so when one wave of at least 80% of the resident slots gives
-    // each CTA at most 2 MiB to stream, that single wave is taken, as full as
-    // the tiles allow (4096 x 16384 fp32: 6.06 -> 6.25 TB/s).  Otherwise the
-    // smallest count whose CTAs fill their waves to at least 90% (more splits
-    // add partial traffic and per-CTA overhead), else the count with the best
-    // wave efficiency: with more data per CTA the fuller waves win (16384 x
-    // 16384 fp32: 7.06 TB/s, 6.89 in one 84% wave).
+    // Row splits (each warp keeps at least U rows).  When the tiles alone
+    // fill at least 80% of the resident slots the rows are not split (no
+    // combine: 4096 x 16384 fp32 in 256 CTAs, 40.0 us; with 4 splits of 64
+    // wider tiles 42.2).  Otherwise a wave of CTAs carries a fixed cost of a
+    // few microseconds (the CTAs' ramp, the split combine), so when one wave
+    // of at least 80% of the resident slots gives each CTA at most 2 MiB to
+    // stream, that single wave is taken, as full as the tiles allow.
+    // Otherwise the smallest count whose CTAs fill their waves to at least 90%
+    // (more splits add partial traffic and per-CTA overhead), else the count
+    // with the best wave efficiency.
     int64_t splits = knob(RED_KNOB_COLPROD_SPLITS);
+    if (splits <= 0 && (double)tiles >= 0.8 * (double)((int64_t)di.sms * occ))
+        splits = 1;
     if (splits <= 0) {
         const int64_t slots = (int64_t)di.sms * occ;
         int64_t smax = R / ((int64_t)CP_WY * U * rpw);

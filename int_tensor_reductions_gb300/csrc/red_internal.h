@@ -64,6 +64,7 @@ int launch_typed_tiny(int op, int dtype, const void *x, int64_t rows, int len, i
 // Column reductions of the R x C region of a row-major matrix with row stride ld >= C.
 int launch_cols(int op, int dtype, const void *x, int64_t R, int64_t C, int64_t ld, void *out, cudaStream_t s);
 
+
 // Kernel launch on stream s with the programmatic-serialization attribute
 // (the kernel's pdl_enter() waits for its predecessors before any global
 // access, so the order of effects is that of a plain launch).

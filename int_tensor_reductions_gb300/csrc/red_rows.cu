@@ -68,11 +68,19 @@ __device__ __forceinline__ float2 ld2p(const float *p)
     return v;
 }
 
-template <int OP, int G, bool RAGGED>
-__global__ void __launch_bounds__(ROWS_NT, 3)
+// Resident CTAs per SM: 3 for the general kernel (<= 85 registers); 4 for
+// dense rows that start on 32-byte boundaries (ALIGNED: no head or tail
+// pieces, so the lean body fits 64 registers and a lane keeps the same four
+// blocks in flight with a third more lanes per SM).
+template <bool ALIGNED>
+constexpr int rows_min_ctas() { return ALIGNED ? 4 : 3; }
+
+template <int OP, int G, bool RAGGED, bool ALIGNED = false>
+__global__ void __launch_bounds__(ROWS_NT, rows_min_ctas<ALIGNED>())
 rows_kernel(const float *__restrict__ x, const int64_t *__restrict__ off, int64_t rows, int64_t len,
             int64_t nnz, int accum, float *__restrict__ out)
 {
+    static_assert(!(ALIGNED && RAGGED), "ragged rows start anywhere");
     pdl_enter();
     constexpr int GPW = 32 / G;           // rows per warp at a time
     constexpr int U = ROWS_U;              // blocks in flight per lane
@@ -145,9 +153,24 @@ rows_kernel(const float *__restrict__ x, const int64_t *__restrict__ off, int64_
             // lengths so that every piece is naturally aligned.  Every load
             // lies inside the row.
             const int64_t e = b + L;
-            const int64_t a = ((b + x_mis + 7) & ~int64_t(7)) - x_mis;
-            const int64_t z = ((e + x_mis) & ~int64_t(7)) - x_mis;
-            if (a <= z) {
+            const int64_t a = ALIGNED ? b : ((b + x_mis + 7) & ~int64_t(7)) - x_mis;
+            const int64_t z = ALIGNED ? e : ((e + x_mis) & ~int64_t(7)) - x_mis;
+            if (ALIGNED) {
+                // every row is whole 32-byte blocks from an aligned start
+                const int64_t nfull = L >> 3;
+                const float *q = x + b;
+                for (int64_t c0 = gl; c0 < nfull; c0 += (int64_t)U * G) {
+                    float v[U][8];
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        if (c0 + u * G < nfull)
+                            ld8(q + 8 * (c0 + u * G), v[u]);
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        if (c0 + u * G < nfull)
+                            f.chunk(v[u]);
+                }
+            } else if (a <= z) {
                 float hs = ident, ts = ident;
                 float2 h2 = make_float2(ident, ident), t2 = h2;
                 float4 h4 = make_float4(ident, ident, ident, ident), t4 = h4;
@@ -212,12 +235,12 @@ rows_kernel(const float *__restrict__ x, const int64_t *__restrict__ off, int64_
     }
 }
 
-template <int OP, int G, bool RAGGED>
+template <int OP, int G, bool RAGGED, bool ALIGNED>
 int launch_group(const float *x, const int64_t *off, int64_t rows, int64_t len, int64_t nnz, int accum,
                  float *out, cudaStream_t s, int sms)
 {
     static std::atomic<int> occ_cache{0};
-    const int occ = cached_occupancy(occ_cache, (const void *)rows_kernel<OP, G, RAGGED>, ROWS_NT);
+    const int occ = cached_occupancy(occ_cache, (const void *)rows_kernel<OP, G, RAGGED, ALIGNED>, ROWS_NT);
     if (occ <= 0)
         return fail(RED_ECUDA, "row kernel cannot be resident on this device");
     const int64_t rows_per_cta = (int64_t)(ROWS_NT / 32) * (32 / G);
@@ -227,34 +250,34 @@ int launch_group(const float *x, const int64_t *off, int64_t rows, int64_t len, 
         ctas = cap;
     if (ctas < 1)
         ctas = 1;
-    const cudaError_t e = launch_pdl(rows_kernel<OP, G, RAGGED>, dim3((unsigned)ctas), dim3(ROWS_NT), s, x, off, rows,
-                                     len, nnz, accum, out);
+    const cudaError_t e = launch_pdl(rows_kernel<OP, G, RAGGED, ALIGNED>, dim3((unsigned)ctas), dim3(ROWS_NT), s, x,
+                                     off, rows, len, nnz, accum, out);
     count_launches(1);
     return cuda_fail(e != cudaSuccess ? e : cudaGetLastError(), "row kernel launch");
 }
 
-template <int OP, bool RAGGED>
+template <int OP, bool RAGGED, bool ALIGNED>
 int launch_g(int G, const float *x, const int64_t *off, int64_t rows, int64_t len, int64_t nnz, int accum,
              float *out, cudaStream_t s, int sms)
 {
     switch (G) {
-    case 1: return launch_group<OP, 1, RAGGED>(x, off, rows, len, nnz, accum, out, s, sms);
-    case 2: return launch_group<OP, 2, RAGGED>(x, off, rows, len, nnz, accum, out, s, sms);
-    case 4: return launch_group<OP, 4, RAGGED>(x, off, rows, len, nnz, accum, out, s, sms);
-    case 8: return launch_group<OP, 8, RAGGED>(x, off, rows, len, nnz, accum, out, s, sms);
-    case 16: return launch_group<OP, 16, RAGGED>(x, off, rows, len, nnz, accum, out, s, sms);
-    default: return launch_group<OP, 32, RAGGED>(x, off, rows, len, nnz, accum, out, s, sms);
+    case 1: return launch_group<OP, 1, RAGGED, ALIGNED>(x, off, rows, len, nnz, accum, out, s, sms);
+    case 2: return launch_group<OP, 2, RAGGED, ALIGNED>(x, off, rows, len, nnz, accum, out, s, sms);
+    case 4: return launch_group<OP, 4, RAGGED, ALIGNED>(x, off, rows, len, nnz, accum, out, s, sms);
+    case 8: return launch_group<OP, 8, RAGGED, ALIGNED>(x, off, rows, len, nnz, accum, out, s, sms);
+    case 16: return launch_group<OP, 16, RAGGED, ALIGNED>(x, off, rows, len, nnz, accum, out, s, sms);
+    default: return launch_group<OP, 32, RAGGED, ALIGNED>(x, off, rows, len, nnz, accum, out, s, sms);
     }
 }
 
-template <bool RAGGED>
+template <bool RAGGED, bool ALIGNED = false>
 int launch_op(int op, int G, const float *x, const int64_t *off, int64_t rows, int64_t len, int64_t nnz,
               int accum, float *out, cudaStream_t s, int sms)
 {
     switch (op) {
-    case OP_SUM: return launch_g<OP_SUM, RAGGED>(G, x, off, rows, len, nnz, accum, out, s, sms);
-    case OP_MAX: return launch_g<OP_MAX, RAGGED>(G, x, off, rows, len, nnz, accum, out, s, sms);
-    default: return launch_g<OP_MIN, RAGGED>(G, x, off, rows, len, nnz, accum, out, s, sms);
+    case OP_SUM: return launch_g<OP_SUM, RAGGED, ALIGNED>(G, x, off, rows, len, nnz, accum, out, s, sms);
+    case OP_MAX: return launch_g<OP_MAX, RAGGED, ALIGNED>(G, x, off, rows, len, nnz, accum, out, s, sms);
+    default: return launch_g<OP_MIN, RAGGED, ALIGNED>(G, x, off, rows, len, nnz, accum, out, s, sms);
     }
 }
 
@@ -295,6 +318,10 @@ int launch_rows(int op, const float *x, int64_t rows, int64_t len, int accum, fl
         (rows < (int64_t)di.sms * 16 || (len >= 32768 && rows > (int64_t)di.sms * 24 && rows <= 65535)))
         return launch_rows_split(op, x, rows, len, accum, out, s, di);
     const int g = knob(RED_KNOB_ROWS_GROUP) ? knob(RED_KNOB_ROWS_GROUP) : auto_group(len);
+    // Rows of whole 32-byte blocks from a 32-byte aligned x: the lean body at
+    // 4 CTAs per SM (unless the knob asks for the general kernel).
+    if (knob(RED_KNOB_ROWS_ALIGNED) != 2 && (((uintptr_t)x) & 31u) == 0 && len % 8 == 0)
+        return launch_op<false, true>(op, g, x, nullptr, rows, len, 0, accum, out, s, di.sms);
     return launch_op<false>(op, g, x, nullptr, rows, len, 0, accum, out, s, di.sms);
 }
 

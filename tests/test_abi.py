@@ -94,6 +94,23 @@ def test_cols_ld_rejects_and_returns_early(lib):
     assert lib.red_cols_ld(3, RED_F32, None, 4, 0, 16, None, None) == RED_OK
 
 
+def test_element_count_limit_is_2_pow_44(lib):
+    """Every element count is at most 2^44 (include/red.h, "Sizes"); one
+    more is refused on the host, before any CUDA call."""
+    from int_tensor_reductions_gb300 import RED_EINVAL, RED_F32, RED_SUM
+    big = (1 << 44) + 1
+    assert lib.red_full(RED_SUM, 0x1000, big, 0x2000, None) == RED_EINVAL
+    assert "out of range" in _err(lib)
+    assert lib.red_full_noalloc(RED_SUM, 0x1000, big, 0x2000, None) == RED_EINVAL
+    assert lib.red_full_stats(0x1000, big, 0x2000, None) == RED_EINVAL
+    assert lib.red_full_typed(RED_SUM, RED_F32, 0x1000, big, 0x2000, None) == RED_EINVAL
+    assert lib.red_rows(RED_SUM, 0x1000, 1, big, 0, 0x2000, None) == RED_EINVAL
+    assert lib.red_rows(RED_SUM, 0x1000, (1 << 22) + 1, 1 << 22, 0, 0x2000, None) == RED_EINVAL
+    assert lib.red_rows_typed(RED_SUM, RED_F32, 0x1000, big, 1, 0, 0x2000, None) == RED_EINVAL
+    assert lib.red_rows_ragged(RED_SUM, 0x1000, 0x3000, 4, big, 0, 0x2000, None) == RED_EINVAL
+    assert lib.red_cols(RED_SUM, RED_F32, 0x1000, (1 << 30) + 1, 1 << 14, 0x2000, None) == RED_EINVAL
+
+
 def test_knobs_and_modes(lib):
     import int_tensor_reductions_gb300 as itr
     assert lib.red_set_full_mode(9) == itr.RED_EINVAL

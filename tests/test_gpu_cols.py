@@ -32,6 +32,7 @@ def _lib():
     lib_ready()
     yield
     itr.red_set_knob(itr.RED_KNOB_COLPROD_SPLITS, 0)
+    itr.red_set_knob(itr.RED_KNOB_COLS_LANES, 0)
 
 
 def _decode(t: torch.Tensor, dtype: str) -> np.ndarray:
@@ -113,6 +114,26 @@ def test_tall_wide_and_ragged_tiles(R, C, dtype):
     for op in ("prod", "sum", "max"):
         x = synth.col_input(op, dtype, (R, C), R + C, device="cuda")
         check_cols(op, dtype, x, f"{op} {dtype} {R}x{C}")
+
+
+@pytest.mark.parametrize("lanes", [1, 2, 4, 8, 16, 32])
+def test_every_lanes_per_row_setting(lanes):
+    """Column tiles of 1 to 32 lanes per row (the automatic choice takes 8
+    for matrices of many rows, 32 for short ones), with the automatic and a
+    forced split count."""
+    itr.red_set_knob(itr.RED_KNOB_COLS_LANES, lanes)
+    try:
+        for dtype in ("f32", "i32", "bf16", "u16"):
+            for op, (R, C) in (("prod", (300, 1032)), ("sum", (2000, 520)), ("max", (64, 4104)), ("min", (3, 136))):
+                x = synth.col_input(op, dtype, (R, C), R + lanes, device="cuda")
+                check_cols(op, dtype, x, f"{op} {dtype} {R}x{C} lanes={lanes}")
+                itr.red_set_knob(itr.RED_KNOB_COLPROD_SPLITS, 5)
+                try:
+                    check_cols(op, dtype, x, f"{op} {dtype} {R}x{C} lanes={lanes} splits=5")
+                finally:
+                    itr.red_set_knob(itr.RED_KNOB_COLPROD_SPLITS, 0)
+    finally:
+        itr.red_set_knob(itr.RED_KNOB_COLS_LANES, 0)
 
 
 def test_int_wrap_closed_forms():

@@ -1,7 +1,8 @@
 """Seeded random cases of the entry points against the oracle: sizes,
 base alignments, operators, element types, accum, row strides and every
-mapping choice (grid stage, lanes per row, ragged mapping, column row
-splits) drawn at random, so that combinations the hand-picked shapes of the
+mapping choice (grid stage, lanes per row, aligned or general row kernel,
+ragged mapping, column row splits and lanes per column-tile row) drawn at
+random, so that combinations the hand-picked shapes of the
 other files do not name are covered too.  Same tolerances as those files:
 integer and max / min results bit for bit, fp32 sums within 1e-5 * sum|x|,
 fp32 products within 5e-4 relative, half and bfloat16 within one unit in
@@ -34,7 +35,7 @@ def _lib():
 def _reset():
     itr.red_set_full_mode(itr.RED_MODE_AUTO)
     for k in (itr.RED_KNOB_ROWS_GROUP, itr.RED_KNOB_RAGGED_GROUP, itr.RED_KNOB_COLPROD_SPLITS,
-              itr.RED_KNOB_RAGGED_STAGED):
+              itr.RED_KNOB_RAGGED_STAGED, itr.RED_KNOB_ROWS_ALIGNED, itr.RED_KNOB_COLS_LANES):
         itr.red_set_knob(k, 0)
 
 
@@ -79,12 +80,14 @@ def test_rows(case):
                  shift).view(rows, length)
     dst = synth.uniform((rows,), -1.0, 1.0, case + 1, device="cuda")
     xh, dh = to_host(x), to_host(dst)
+    aligned = int(gen.choice([0, 2]))  # 2: the general row kernel even for rows of whole 32-byte blocks
     itr.red_set_knob(itr.RED_KNOB_ROWS_GROUP, g)
+    itr.red_set_knob(itr.RED_KNOB_ROWS_ALIGNED, aligned)
     try:
         for op in OPS3:
             out = dst.clone()
             itr.red_rows(op, x, accum=accum, out=out)
-            what = f"case {case}: {rows}x{length} shift={shift} G={g} accum={accum} {op}"
+            what = f"case {case}: {rows}x{length} shift={shift} G={g} aligned={aligned} accum={accum} {op}"
             if op == "sum":
                 s, a = oracle.rows("sum", xh, rows, length, accum, dh)
                 check_sum(to_host(out), s, a, what)
@@ -141,9 +144,12 @@ def test_cols(case):
     splits = int(gen.choice([0, 0, 1, 2, 7, 64]))
     full = synth.col_input(op, dtype, (R * ld + shift,), case, device="cuda")
     x = full[shift:].view(R, ld)[:, :C]
+    lanes = int(gen.choice([0, 0, 1, 2, 4, 8, 16, 32]))
     itr.red_set_knob(itr.RED_KNOB_COLPROD_SPLITS, splits)
+    itr.red_set_knob(itr.RED_KNOB_COLS_LANES, lanes)
     try:
-        check_cols(op, dtype, x, f"case {case}: {op} {dtype} {R}x{C} ld={ld} shift={shift} splits={splits}")
+        check_cols(op, dtype, x,
+                   f"case {case}: {op} {dtype} {R}x{C} ld={ld} shift={shift} splits={splits} lanes={lanes}")
     finally:
         _reset()
 

@@ -22,6 +22,7 @@ def _lib():
     yield
     itr.red_set_knob(itr.RED_KNOB_ROWS_GROUP, 0)
     itr.red_set_knob(itr.RED_KNOB_RAGGED_GROUP, 0)
+    itr.red_set_knob(itr.RED_KNOB_ROWS_ALIGNED, 0)
 
 
 def _dense_case(x2d: torch.Tensor, dst: torch.Tensor, what: str):
@@ -61,6 +62,23 @@ def test_dense_every_group_size(g):
             _dense_case(x[3:].view(rows, length), dst, f"G={g} {rows}x{length}")
     finally:
         itr.red_set_knob(itr.RED_KNOB_ROWS_GROUP, 0)
+
+
+@pytest.mark.parametrize("aligned", [0, 2])
+def test_dense_whole_block_rows_both_kernels(aligned):
+    """Rows of whole 32-byte blocks from a 32-byte aligned base go to the
+    aligned row kernel; knob value 2 sends the same rows to the general one.
+    Both against the oracle, at every lanes-per-row setting the automatic
+    choice gives for these lengths."""
+    itr.red_set_knob(itr.RED_KNOB_ROWS_ALIGNED, aligned)
+    try:
+        for rows, length in ((3, 72), (1000, 64 + 8), (257, 256), (4099, 1024), (33, 4096), (5, 65536)):
+            x = synth.normal((rows, length), rows + length, device="cuda")
+            assert x.data_ptr() % 32 == 0
+            dst = synth.uniform((rows,), -1.0, 1.0, 5, device="cuda")
+            _dense_case(x, dst, f"aligned={aligned} {rows}x{length}")
+    finally:
+        itr.red_set_knob(itr.RED_KNOB_ROWS_ALIGNED, 0)
 
 
 def test_dense_len0():

@@ -13,8 +13,8 @@
 //       every further full chunk of 8 is added with four packed
 //       add.rn.ftz.f32x2; a remainder of r < 8 elements is added one at a
 //       time into slots 0..r-1; the accumulator then collapses 8 -> 4 -> 2
-//       -> 1 with three packed adds and one scalar add.  N < 8 (below the
-//       page's dispatch gate): a left-to-right scalar fold.  The rounding
+//       -> 1 (collapse8: three packed adds and one scalar add).  N < 8
+//       (below the page's dispatch gate): a left-to-right scalar fold.  The rounding
 //       order is therefore fixed by N alone: the same a gives the same bits
 //       on every launch configuration.
 //   red_dev::thread_max<N>, thread_min<N>  a 4-wide accumulator loaded from
@@ -41,6 +41,29 @@ __device__ __forceinline__ float2 add_f32x2(float2 a, float2 b)
         : "=f"(d.x), "=f"(d.y)
         : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
     return d;
+}
+
+// The collapse of an 8-wide packed accumulator (four float2 slots) to one
+// float: a pairwise tree over the slots, each level adding slot k + h into
+// slot k for h = 1, then 2 (the pairing the page's "Algorithm" prescribes:
+// lanes (0,1) gain (2,3) and (4,5) gain (6,7), then (0,1) gains (4,5)), and
+// a final scalar add of the two lanes left: round-to-nearest, or with FTZ
+// also flushing a denormal result to zero (add.rn.ftz.f32).
+template <bool FTZ = false>
+__device__ __forceinline__ float collapse8(float2 (&s)[4])
+{
+#pragma unroll
+    for (int h = 1; h < 4; h *= 2)
+#pragma unroll
+        for (int k = 0; k < 4; k += 2 * h)
+            s[k] = add_f32x2(s[k], s[k + h]);
+    if constexpr (FTZ) {
+        float d;
+        asm("add.rn.ftz.f32 %0, %1, %2;" : "=f"(d) : "f"(s[0].x), "f"(s[0].y));
+        return d;
+    } else {
+        return __fadd_rn(s[0].x, s[0].y);
+    }
 }
 
 // Three-input max / min (the max3.f32 / min3.f32 of the page).
@@ -91,10 +114,7 @@ __device__ __forceinline__ float thread_sum(const float (&a)[N], bool accum = fa
             else
                 s[j >> 1].x = __fadd_rn(s[j >> 1].x, a[i]);
         }
-        s[0] = add_f32x2(s[0], s[1]);  // (0,1) += (2,3)
-        s[2] = add_f32x2(s[2], s[3]);  // (4,5) += (6,7)
-        s[0] = add_f32x2(s[0], s[2]);  // (0,1) += (4,5)
-        return __fadd_rn(s[0].x, s[0].y);
+        return collapse8(s);
     }
 }
 

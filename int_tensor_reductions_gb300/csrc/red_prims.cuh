@@ -156,10 +156,8 @@ struct Fold<OP_SUM> {
     }
     __device__ __forceinline__ float finish() const
     {
-        float2 s01 = add_f32x2(a[0], a[1]);  // (0,1) + (2,3)
-        float2 s45 = add_f32x2(a[2], a[3]);  // (4,5) + (6,7)
-        float2 s = add_f32x2(s01, s45);
-        return add_ftz(s.x, s.y);
+        float2 s[4] = {a[0], a[1], a[2], a[3]};
+        return red_dev::collapse8<true>(s);
     }
 };
 

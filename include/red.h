@@ -202,7 +202,9 @@ int red_rows_thread(int op, const float *x, int64_t rows, int len, int accum, fl
  *            clamps every offset to [0, nnz] (a decreasing pair reads as an
  *            empty row), so it never reads outside x[0 .. nnz), but the
  *            results of invalid offsets are unspecified.
- *   rows     number of rows, >= 0.   nnz  number of values in x, >= 0.
+ *   rows     number of rows, >= 0.
+ *   nnz      number of values in x, >= 0 (passed by the caller: reading
+ *            offsets[rows] from device memory would need a synchronise).
  *   out      device pointer to rows floats (read first when accum != 0).
  * An empty row gives 0 for RED_SUM, -inf for RED_MAX and +inf for RED_MIN
  * (the identity of the fold); with accum the old out[r] is kept.

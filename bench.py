@@ -298,6 +298,11 @@ class Workload:
             "colprod4b": 4 * self.x4b.numel() + 4 * self.x4b.shape[1],
             "ragged5": 4 * nnz5 + 8 * (n5 + 1) + 4 * n5,
         }
+        # input elements each op reduces (for elements per second)
+        self.elems_of = {
+            "full1": self.x1.numel(), "full3": self.x3.numel(), "rows2": r2 * l2, "rows2_accum": r2 * l2,
+            "colprod4a": self.x4a.numel(), "colprod4b": self.x4b.numel(), "ragged5": nnz5,
+        }
         # step order: interleaved so that no buffer is re-read while hot
         self.plan = [
             ("full1 sum", "full1"), ("full3 sum", "full3"), ("rows2 sum", "rows2"), ("ragged5 sum", "ragged5"),
@@ -519,6 +524,7 @@ def run_ours(args):
             "parallelism": f"replicas x{world}",
         },
         "frac_of_nominal_8TBs": round(value / world / NOMINAL_HBM_GBS, 4),
+        "gelem_s": round(world * sum(w.elems_of[k] for _, k in w.plan) * K / (total_ms * 1e-3) / 1e9, 2),
         "roofline": {
             "bound": "hbm", "kernel": DOMINANT, "achieved": achieved and round(achieved, 1), "peak": peak,
             "unit": "GB/s", "frac": achieved and round(achieved / peak, 4), "peak_source": peak_src,
@@ -559,14 +565,18 @@ def run_ours(args):
     return 0
 
 
-def per_op_graphs(w, stream, calls_per_replay=16, replays=6):
+def per_op_graphs(w, stream, calls_per_replay=16, replays=8):
     """Device time per call of every op of the step, each timed alone: one
-    CUDA graph per op holding ``calls_per_replay`` back-to-back calls, over
-    copies of that op's inputs (so that every call reads its input cold: the
-    copies together exceed three times the L2; a replay calls every copy once), replayed ``replays`` times between
-    two events on the launching stream.  Graph replay leaves no host launch
-    gap, and programmatic dependent launch overlaps each call's launch with
-    its predecessor's drain, as in the timed region."""
+    CUDA graph per op holding at least ``calls_per_replay`` back-to-back calls
+    over copies of that op's inputs (so that every call reads its input cold:
+    the copies together exceed three times the L2; a replay calls every copy
+    once), after one warm-up replay ``replays`` replays queued back to back,
+    each between two events on the launching stream.  Graph replay leaves no
+    host launch gap, and programmatic dependent launch overlaps each call's
+    launch with its predecessor's drain, as in the timed region.  Per op: the
+    median and the best replay's time per call, GB/s of algorithmic bytes and
+    input elements per second from the median."""
+    import statistics
     import torch
     import int_tensor_reductions_gb300 as itr
     l2 = torch.cuda.get_device_properties(stream.device).L2_cache_size
@@ -594,7 +604,7 @@ def per_op_graphs(w, stream, calls_per_replay=16, replays=6):
             return [lambda x=x: itr.red_colprod(x, w.o4a) for x in x4as]
         return [lambda x=x: itr.red_colprod(x, w.o4b) for x in x4bs]
 
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(replays + 1)]
     per_op = {}
     for name, key in w.plan:
         f = fns(name)
@@ -608,18 +618,20 @@ def per_op_graphs(w, stream, calls_per_replay=16, replays=6):
                 f[k % len(f)]()
         g.replay()
         torch.cuda.synchronize()
-        e0.record(stream)
-        for _ in range(replays):
+        ev[0].record(stream)
+        for k in range(replays):
             g.replay()
-        e1.record(stream)
+            ev[k + 1].record(stream)
         torch.cuda.synchronize()
-        ms = e0.elapsed_time(e1) / (replays * ncalls)
-        per_op[name] = {"ms": round(ms, 5), "gbs": round(w.bytes_of[key] / (ms * 1e-3) / 1e9, 1)}
+        per_call = [ev[k].elapsed_time(ev[k + 1]) / ncalls for k in range(replays)]
+        ms, best = statistics.median(per_call), min(per_call)
+        per_op[name] = {"ms": round(ms, 5), "gbs": round(w.bytes_of[key] / (ms * 1e-3) / 1e9, 1),
+                        "best_ms": round(best, 5), "gelem_s": round(w.elems_of[key] / (ms * 1e-3) / 1e9, 2)}
         del g
     del x1s, x2s, x4as, x4bs, x3s, x5s
     torch.cuda.empty_cache()
     note = (f"graph-timed per op: at least {calls_per_replay} back-to-back calls per CUDA graph over copies of the "
-            f"op's inputs (each call reads cold), {replays} replays between two events")
+            f"op's inputs (each call reads cold); median (ms, gbs, gelem_s) and best of {replays} replays")
     return per_op, note
 
 

@@ -14,8 +14,9 @@
 // Layout of the work: a CTA of 16 warps owns a tile of lpr*V adjacent
 // columns, lpr lanes per row (8 for matrices of many rows, 32 for short ones,
 // or the power of two that covers a narrower matrix; the warps take 32/lpr
-// consecutive rows per step, so no lane idles).  Each lane owns V adjacent columns and keeps V running
-// accumulators (per-thread column accumulators); the lane groups of warp w
+// consecutive rows per step, so no lane idles).  Each lane owns V adjacent
+// columns and keeps V running accumulators (per-thread column
+// accumulators); the lane groups of warp w
 // walk rows i0 + w*32/lpr, ... in steps of 16*32/lpr rows, each lane reading
 // 32 bytes of a row per load (16 bytes for 16-bit types, whose lanes then
 // keep 8 rows in flight instead of 4; coalesced, row-major order kept).  The

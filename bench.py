@@ -224,6 +224,14 @@ def _case_inputs(name, dev):
         x = synth.col_input("sum", "bf16", (131072, 1024), 14, dev)
         o = torch.empty(1024, dtype=x.dtype, device=dev)
         return (lambda: itr.red_cols("sum", x, o)), 2 * x.numel() + 2 * 1024
+    if name == "rows_262144x1024":
+        x = synth.normal((262144, 1024), 7, dev)
+        o = torch.empty(262144, device=dev)
+        return (lambda: itr.red_rows("sum", x, out=o)), 4 * x.numel() + 4 * 262144
+    if name == "colprod_16384x16384":
+        x = synth.uniform((16384, 16384), 0.999, 1.001, 8, dev)
+        o = torch.empty(16384, device=dev)
+        return (lambda: itr.red_colprod(x, o)), 4 * x.numel() + 4 * 16384
     if name == "ragged_short_2p25":
         off = synth.ragged_offsets(1 << 25, 2, 6, 15, dev)
         nnz = int(off[-1].item())
@@ -235,7 +243,7 @@ def _case_inputs(name, dev):
 
 CASES = ("stats_full_2p28", "stats_rows_65536x1024", "thread_rows_2p22x32", "cols_f16_prod_4096x16384",
          "typed_full_f16_max_2p29", "typed_rows_bf16_max_65536x2048", "typed_rows_u16_max_2p24x8",
-         "cols_bf16_sum_131072x1024", "ragged_short_2p25")
+         "cols_bf16_sum_131072x1024", "ragged_short_2p25", "rows_262144x1024", "colprod_16384x16384")
 
 
 def run_case(args):

@@ -9,7 +9,9 @@
 // device address (a kernel given it would fault, or on a GPU that can reach
 // host memory silently use the wrong memory).  The device address is looked
 // up once per device with cudaGetSymbolAddress, with that device current,
-// and cached.
+// and cached; a cudaDeviceReset unloads the module and makes the cached
+// address stale, so the call must not be used on that device afterwards
+// (red.h states this limit for the caller).
 #include <mutex>
 
 #include "red.h"
